@@ -1,0 +1,408 @@
+"""Benchmark of the hot path: BlockMask creation + block-sparse masked attention forward (and the paged
+split-KV decode as a secondary line item), on seeded synthetic inputs, through the C ABI.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload cfg2|cfg3|cfg4]
+
+A step = fa_create_block_mask + fa_flex_forward over the whole workload (default: plain causal, B=4,
+Hq=Hkv=16, N=4096, d=128, 128x128 blocks). value = physical TFLOP/s (4*d*Bq*Bk per visited block per
+(b,h)) of the whole step, all ranks. One JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-sparse attn fwd TFLOP/s (% BF16 tc peak); decode KV GB/s (% HBM)"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="cfg2", choices=["cfg2", "cfg3", "cfg4"])
+    p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return dict(hbm=float(m["hbm_gbs"]), bf16=float(m["bf16_tflops"]),
+                    bf16_sus=float(m.get("bf16_tflops_sustained", m["bf16_tflops"])), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def make_workload(name):
+    from block_sparse_masked_create_gb300 import workloads
+    return {"cfg2": workloads.cfg2, "cfg3": workloads.cfg3, "cfg4": workloads.cfg4}[name]()
+
+
+def visited_blocks(w):
+    """Visited (full + partial) blocks per mask row, from the oracle-free block counts of the device table."""
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.samples = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in self.samples:
+            try:
+                sm.append(float(s[1]))
+                mx = float(s[2])
+                for n, v in zip(names, s[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+            except Exception:
+                pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------------
+# reference arm / CPU baseline: the fp64 oracle as it stands, on a bounded sample, on host cores
+# ------------------------------------------------------------------------------------------------------
+CPU_SNIPPET = r"""
+import json, sys, time, numpy as np
+sys.path.insert(0, %(root)r)
+from block_sparse_masked_create_gb300 import workloads, synth
+from oracle import flexmask_oracle as orc
+w = workloads.%(wl)s()
+rng = np.random.default_rng(0)
+g = w.Hq // w.Hkv
+n_q = -(-w.q_len // w.bq)
+times, flops = [], []
+for it in range(%(reps)d):
+    b, h, r = int(rng.integers(w.B)), int(rng.integers(w.Hq)), int(rng.integers(n_q))
+    rows = np.arange(r * w.bq, min(w.q_len, (r + 1) * w.bq))
+    hk = h // g
+    # inputs of this sample only (generator slices: counter based)
+    qb = synth.normal_bf16_bits(w.seed, 1, (len(rows), w.d), first=((b * w.Hq + h) * w.q_len + rows[0]) * w.d)
+    kb = synth.normal_bf16_bits(w.seed, 2, (w.kv_len, w.d), first=(b * w.Hkv + hk) * w.kv_len * w.d)
+    vb = synth.normal_bf16_bits(w.seed, 3, (w.kv_len, w.d), first=(b * w.Hkv + hk) * w.kv_len * w.d)
+    qf, kf, vf = (synth.bf16_bits_to_f64(x) for x in (qb, kb, vb))
+    t = orc.block_mask(w.rule, 1, 1, w.q_len, w.kv_len, w.bq, w.bk, doc_ids=w.doc_ids, rows=[r])
+    vis = int(t["kv_num"][0, 0, r] + t["full_kv_num"][0, 0, r])
+    t0 = time.perf_counter()
+    orc.attention_rows(qf, kf, vf, w.rule, rows, b, h, w.q_len, w.kv_len, w.scale,
+                       {k: (np.asarray(v, np.float64) if k != 'softcap' else v) for k, v in w.score.items()},
+                       0, w.doc_ids)
+    times.append(time.perf_counter() - t0)
+    flops.append(4.0 * w.d * w.bq * w.bk * vis)
+print(json.dumps({"times": times, "flops": flops}))
+"""
+
+
+def run_oracle_sample(wl: str, reps: int) -> dict:
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    code = CPU_SNIPPET % dict(root=ROOT, wl=wl, reps=reps)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def reference_arm(args, rank):
+    if rank != 0:
+        return
+    w = make_workload(args.workload)
+    reps = args.warmup + args.steps
+    res = run_oracle_sample(args.workload, reps)
+    t = res["times"][args.warmup:]
+    f = res["flops"][args.warmup:]
+    value = sum(f) / sum(t) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(t) / len(t), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} N={w.q_len} d={w.d} Bq=Bk={w.bq}",
+                   "step": "oracle on one query block row (Bq rows) of a random (b, h)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} timed query-block rows of {w.bq} queries (fp64 numpy, 1 thread)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------------
+def ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from block_sparse_masked_create_gb300 import fa, workloads
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pk = peaks()
+    w = make_workload(args.workload).generate()
+    q = workloads.bf16_torch(w.q_bits, dev)
+    k = workloads.bf16_torch(w.k_bits, dev)
+    v = workloads.bf16_torch(w.v_bits, dev)
+    doc = None if w.doc_ids is None else torch.from_numpy(w.doc_ids.astype(np.int32)).to(dev)
+    al = None
+    if w.score.get("alibi_slopes") is not None:
+        al = torch.tensor(np.asarray(w.score["alibi_slopes"], np.float32), device=dev)
+    sc = fa.make_score_rule(al, None, w.score.get("softcap", 0.0))
+    rule = fa.make_mask_rule(w.rule, doc_ids=doc)
+    bm = fa.create_block_mask(rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk, device=dev, keep=[doc])
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stats = fa.block_mask_stats(bm).cpu().tolist()
+    heads = w.B * w.Hq // (bm.c.Bm * bm.c.Hm)
+    visited = (stats[0] + stats[1]) * heads
+    phys_flops = 4.0 * w.d * w.bq * w.bk * visited
+    # logical pairs: exact count from the rule (oracle-free; closed forms of the configs' rules)
+    logical_pairs = None
+    if args.workload == "cfg2":
+        logical_pairs = w.B * w.Hq * w.q_len * (w.q_len + 1) // 2
+    elif args.workload == "cfg4":
+        W = 1024
+        logical_pairs = w.B * w.Hq * (W * (W + 1) // 2 + (w.q_len - W) * W)
+    elif args.workload == "cfg3":
+        logical_pairs = w.B * w.Hq * int(sum(int(L) * (int(L) + 1) // 2 for L in w.doc_lens))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.recreate_block_mask(bm, rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk)
+        fa.flex_forward(q, k, v, bm, sc, w.scale, out=out, lse=lse, status=status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.check_status(status) != fa.OK:
+        raise RuntimeError("device status after warm-up")
+    # per-kernel time of the dominant kernel (the forward) with events on the launching stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t0 = time.perf_counter()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            fa.recreate_block_mask(bm, rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk)
+            ev[i][1].record(stream)
+            fa.flex_forward(q, k, v, bm, sc, w.scale, out=out, lse=lse, status=status)
+            ev[i][2].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if dist:
+        dist.barrier()
+    ms = start.elapsed_time(end)
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    fwd_ms = [a.elapsed_time(c) for (_, a, c) in ev]
+    mask_ms = [s.elapsed_time(a) for (s, a, _) in ev]
+    st_code = fa.check_status(status)
+    ms_step = ms / args.steps
+    value = world * phys_flops / (ms_step * 1e-3) / 1e12
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    achieved = phys_flops / (fwd_avg * 1e-3) / 1e12
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if rank == 0 or world > 1:
+        hq = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True).copy_(q)
+        hk = torch.empty(k.shape, dtype=torch.bfloat16, pin_memory=True).copy_(k)
+        hv = torch.empty(v.shape, dtype=torch.bfloat16, pin_memory=True).copy_(v)
+        ho = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=torch.float32, pin_memory=True)
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            fa.recreate_block_mask(bm, rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk)
+            fa.flex_forward(q, k, v, bm, sc, w.scale, out=out, lse=lse, status=status)
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(max(3, args.warmup // 2)):
+            e2e_step()
+        torch.cuda.synchronize()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n2 = max(3, args.steps // 2)
+        s2.record(stream)
+        for _ in range(n2):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = s2.elapsed_time(e2) / n2
+        bi = 3 * q.numel() * 2
+        bo = out.numel() * 2 + lse.numel() * 4
+        e2e = {"value": world * phys_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
+
+    # ---------------- decode (secondary metric of the same hot path): paged split-KV, 64 requests
+    dec_line = None
+    if not args.no_decode:
+        dec_line = bench_decode(args, dev, pk)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        try:
+            res = run_oracle_sample(args.workload, 6)
+            cpu = {"value": sum(res["flops"]) / sum(res["times"]) / 1e12, "unit": "TFLOP/s", "cores": 1,
+                   "kind": "oracle",
+                   "sample": f"6 query-block rows ({w.bq} queries each) of random (b,h), fp64 numpy, 1 thread; "
+                             f"{sum(res['times']):.1f} s"}
+        except Exception as e:  # reported, never silently replaced
+            cpu = {"value": None, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+
+    traffic = load_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} N={w.q_len} d={w.d} Bq=Bk={w.bq}",
+                   "step": "fa_create_block_mask + fa_flex_forward", "l2": "inputs 3x64 MiB + output > 129 MB L2 "
+                   "(no flush)", "parallelism": f"replica x{world} (independent (b,h) shards, no collective)"},
+        "physical_tflop_per_step": phys_flops / 1e12,
+        "logical_tflops": (world * 4.0 * w.d * logical_pairs / (ms_step * 1e-3) / 1e12) if logical_pairs else None,
+        "pct_bf16_peak": value / world / pk["bf16"],
+        "mask_build_us": 1e3 * statistics.median(mask_ms),
+        "forward_ms_median": statistics.median(fwd_ms),
+        "blocks": {"full": stats[0], "partial": stats[1], "empty": stats[2], "row_max": stats[3],
+                   "visited_total": visited},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": achieved / pk["bf16"], "traffic": traffic,
+                     "kernel": "fa_flex_forward", "peak_src": f"{pk['src']} bf16 burst"},
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": args.steps * 3,
+        "clocks": clk.summary(), "status": fa.status_string(st_code), "wall_s": wall,
+    }
+    if dec_line:
+        line["decode"] = dec_line
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def bench_decode(args, dev, pk):
+    import numpy as np
+    import torch
+
+    from block_sparse_masked_create_gb300 import fa, workloads
+    d = workloads.cfg5().generate()
+    q = workloads.bf16_torch(d.q_bits, dev)
+    kp = workloads.bf16_torch(d.k_bits, dev)
+    vp = workloads.bf16_torch(d.v_bits, dev)
+    pt = torch.from_numpy(d.page_table).to(dev)
+    off = torch.from_numpy(d.q_offset).to(dev)
+    rule = fa.make_mask_rule(d.rule, q_offset=off, batch_dependent=True)
+    bm = fa.create_block_mask(rule, d.Bz, d.Hq, 1, d.kv_len, 1, d.page, device=dev, keep=[off])
+    out = torch.empty_like(q)
+    lse = torch.empty((d.Bz, d.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.decode_workspace_bytes(d.Bz, d.Hq, d.d, d.max_pages, d.page), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        fa.flex_decode(q, kp, vp, pt, bm, None, d.scale, out=out, lse=lse, workspace=ws, status=status)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    n = max(5, args.steps)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        a.record(stream)
+        fa.flex_decode(q, kp, vp, pt, bm, None, d.scale, out=out, lse=lse, workspace=ws, status=status)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    kv_bytes = int(sum(int(L) for L in d.kv_lens)) * d.Hkv * d.d * 2 * 2
+    other = q.numel() * 2 + out.numel() * 2 + lse.numel() * 4 + pt.numel() * 4
+    med = statistics.median(ms)
+    gbs = (kv_bytes + other) / (med * 1e-3) / 1e9
+    return {"workload": "cfg5 paged decode: 64 requests, Hq=32, Hkv=8, d=128, 128-token pages, L~U[1024,32768]",
+            "kv_gb": kv_bytes / 1e9, "ms_median": med, "GB/s": gbs, "pct_hbm": gbs / pk["hbm"],
+            "status": fa.status_string(fa.check_status(status)),
+            "note": "KV read once per KV head; K/V pages 2x%.1f GB > L2" % (d.k_bits.nbytes / 1e9)}
+
+
+def load_traffic(wl):
+    """dram bytes per launch of the forward kernel from the committed ncu summary, if it matches."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            t = json.load(f)
+        return t.get(wl)
+    except Exception:
+        return None
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+    ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

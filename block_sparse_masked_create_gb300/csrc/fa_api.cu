@@ -1,0 +1,450 @@
+// C-ABI layer of libfa.so: argument checks, rule rewriting, BlockMask buffer layout, tensor-map encoding
+// and kernel dispatch. Every check runs on the host before anything is launched.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "fa_launch.h"
+
+namespace fa {
+
+static std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+// ------------------------------------------------------------------------------------------------
+// Rule rewriting: postfix program -> OR of conjunctions (each conjunction one KV interval, optionally
+// intersected with document equality). AND distributes over OR; a conjunction keeps the tightest
+// window and prefix bounds.
+// ------------------------------------------------------------------------------------------------
+struct HTerm {
+  bool causal = false, doc = false;
+  int64_t win = INT64_MAX, pre = INT64_MAX;
+  bool operator==(const HTerm& o) const {
+    return causal == o.causal && doc == o.doc && win == o.win && pre == o.pre;
+  }
+};
+
+static int compile_rule(const fa_mask_rule* r, DevRule* out) {
+  if (!r || r->n_ops < 1 || r->n_ops > FA_MAX_RULE_OPS) return FA_ERR_INVALID_ARG;
+  std::vector<std::vector<HTerm>> st;
+  bool any_doc = false;
+  for (int i = 0; i < r->n_ops; ++i) {
+    HTerm t;
+    switch (r->op[i]) {
+      case FA_M_TRUE: st.push_back({t}); break;
+      case FA_M_CAUSAL: t.causal = true; st.push_back({t}); break;
+      case FA_M_WINDOW: t.win = r->arg[i]; st.push_back({t}); break;
+      case FA_M_PREFIX: t.pre = r->arg[i]; st.push_back({t}); break;
+      case FA_M_DOC: t.doc = true; any_doc = true; st.push_back({t}); break;
+      case FA_M_AND:
+      case FA_M_OR: {
+        if (st.size() < 2) return FA_ERR_INVALID_ARG;
+        std::vector<HTerm> b = st.back();
+        st.pop_back();
+        std::vector<HTerm> a = st.back();
+        st.pop_back();
+        std::vector<HTerm> c;
+        if (r->op[i] == FA_M_OR) {
+          c = a;
+          c.insert(c.end(), b.begin(), b.end());
+        } else {
+          for (const HTerm& x : a)
+            for (const HTerm& y : b) {
+              HTerm z;
+              z.causal = x.causal || y.causal;
+              z.doc = x.doc || y.doc;
+              z.win = std::min(x.win, y.win);
+              z.pre = std::min(x.pre, y.pre);
+              c.push_back(z);
+            }
+        }
+        std::vector<HTerm> u;
+        for (const HTerm& x : c)
+          if (std::find(u.begin(), u.end(), x) == u.end()) u.push_back(x);
+        if (u.size() > 64) return FA_ERR_UNSUPPORTED;
+        st.push_back(u);
+        break;
+      }
+      default: return FA_ERR_INVALID_ARG;
+    }
+  }
+  if (st.size() != 1) return FA_ERR_INVALID_ARG;
+  const std::vector<HTerm>& terms = st.back();
+  if (terms.size() > FA_MAX_RULE_TERMS) return FA_ERR_UNSUPPORTED;
+  if (any_doc && (!r->doc_ids || r->doc_len < 1 || r->doc_batch < 1)) return FA_ERR_INVALID_ARG;
+  if (out) {
+    std::memset(out, 0, sizeof(*out));
+    out->n_terms = (int32_t)terms.size();
+    out->any_doc = 0;
+    for (size_t i = 0; i < terms.size(); ++i) {
+      out->t[i].causal = terms[i].causal;
+      out->t[i].doc = terms[i].doc;
+      out->t[i].win = terms[i].win;
+      out->t[i].pre = terms[i].pre;
+      if (terms[i].doc) out->any_doc = 1;
+    }
+    out->doc_ids = r->doc_ids;
+    out->doc_batch = r->doc_batch;
+    out->doc_len = r->doc_len;
+    out->q_offset = r->q_offset;
+  }
+  return FA_OK;
+}
+
+static DevScore make_score(const fa_score_rule* s, int kv_len) {
+  DevScore d;
+  d.alibi = s ? s->alibi_slopes : nullptr;
+  d.rel = s ? s->rel_bias : nullptr;
+  d.softcap = (s && s->softcap > 0.f) ? s->softcap : 0.f;
+  d.inv_softcap = d.softcap > 0.f ? 1.f / d.softcap : 0.f;
+  d.kv_len = kv_len;
+  return d;
+}
+
+static DevMask dev_mask(const fa_block_mask* m) {
+  DevMask d;
+  d.Bm = m->Bm;
+  d.Hm = m->Hm;
+  d.q_len = m->q_len;
+  d.kv_len = m->kv_len;
+  d.bq = m->bq;
+  d.bk = m->bk;
+  d.nq = m->nq;
+  d.nk = m->nk;
+  d.kv_num = m->kv_num;
+  d.kv_idx = m->kv_idx;
+  d.full_kv_num = m->full_kv_num;
+  d.full_kv_idx = m->full_kv_idx;
+  return d;
+}
+
+// ------------------------------------------------------------------------------------------------
+// BlockMask buffer layout
+// ------------------------------------------------------------------------------------------------
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct MaskLayout {
+  int Bm, Hm, nq, nk;
+  size_t off[9];
+  size_t total;
+};
+
+static int mask_layout(const fa_mask_rule* rule, int B, int H, int Q_LEN, int KV_LEN, int Bq, int Bk,
+                       MaskLayout* L) {
+  if (!rule) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Q_LEN < 1 || KV_LEN < 1) return FA_ERR_SHAPE;
+  if (Bq < 1 || Bq > 128 || Bk < 1 || Bk > 128) return FA_ERR_SHAPE;
+  L->Bm = rule->batch_dependent ? B : 1;
+  L->Hm = rule->head_dependent ? H : 1;
+  L->nq = (Q_LEN + Bq - 1) / Bq;
+  L->nk = (KV_LEN + Bk - 1) / Bk;
+  const size_t heads = (size_t)L->Bm * L->Hm;
+  const size_t rowsz = heads * L->nq * sizeof(int32_t), colsz = heads * L->nk * sizeof(int32_t);
+  const size_t grid = heads * (size_t)L->nq * L->nk;
+  const size_t sizes[9] = {rowsz, rowsz, colsz, colsz, grid * 4, grid * 4, grid * 4, grid * 4, grid};
+  size_t o = 0;
+  for (int i = 0; i < 9; ++i) {
+    L->off[i] = o;
+    o += align256(sizes[i]);
+  }
+  L->total = o;
+  return FA_OK;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Tensor maps
+// ------------------------------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+  if (!enc) return -1;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int decode_pages_per_split(int page, int max_pages) {
+  int ps = std::max(1, 2048 / std::max(page, 1));
+  return std::min(ps, std::max(max_pages, 1));
+}
+
+static int check_forward(const void* q, const void* k, const void* v, const fa_block_mask* bm, void* out,
+                         float* lse, int B, int Hq, int Hkv, int Q_LEN, int KV_LEN, int d) {
+  if (!q || !k || !v || !bm || !out || !lse) return FA_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Q_LEN < 1 || KV_LEN < 1) return FA_ERR_SHAPE;
+  if (Hq % Hkv) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (bm->q_len != Q_LEN || bm->kv_len != KV_LEN) return FA_ERR_SHAPE;  // never trimmed silently
+  if (!(bm->Bm == 1 || bm->Bm == B) || !(bm->Hm == 1 || bm->Hm == Hq)) return FA_ERR_SHAPE;
+  if (bm->nq != (Q_LEN + bm->bq - 1) / bm->bq || bm->nk != (KV_LEN + bm->bk - 1) / bm->bk) return FA_ERR_SHAPE;
+  auto okb = [](int x) { return x == 16 || x == 32 || x == 64 || x == 128; };
+  if (!okb(bm->bq) || !okb(bm->bk)) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FA_ERR_INVALID_ARG;
+  if (!bm->kv_num || !bm->kv_idx || !bm->full_kv_num || !bm->full_kv_idx) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+static int forward_impl(bool force_mma, const void* q, const void* k, const void* v, const fa_block_mask* bm,
+                        const fa_score_rule* score, float scale, void* out, float* lse, int32_t B, int32_t Hq,
+                        int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d, int32_t* dev_status,
+                        int64_t* dev_counters, fa_stream_t stream) {
+  int s = check_forward(q, k, v, bm, out, lse, B, Hq, Hkv, Q_LEN, KV_LEN, d);
+  if (s != FA_OK) return s;
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  s = compile_rule(&bm->rule, &a.rule);
+  if (s != FA_OK) return s;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.q_len = Q_LEN;
+  a.kv_len = KV_LEN;
+  a.d = d;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt((float)d);
+  a.score = make_score(score, KV_LEN);
+  a.mask = dev_mask(bm);
+  a.status = dev_status;
+  a.counters = dev_counters;
+  a.timeout_ns = g_timeout_ns.load();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!force_mma && bm->bq == 128 && bm->bk == 128) {
+    int r = launch_fwd_tc5(a, st);
+    if (r != FA_ERR_UNSUPPORTED) return r;
+  }
+  return launch_fwd_mma(a, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_SHAPE: return "inconsistent shapes";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device wait timed out";
+    case FA_ERR_DEVICE_CHECK: return "device-side index check failed";
+    case FA_ERR_BUFFER_TOO_SMALL: return "buffer too small";
+  }
+  return "unknown status";
+}
+
+const char* fa_version(void) { return "libfa 0.1 sm_103a"; }
+
+void fa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+uint64_t fa_get_wait_timeout_ns(void) { return g_timeout_ns.load(); }
+
+size_t fa_block_mask_bytes(const fa_mask_rule* rule, int32_t B, int32_t H, int32_t Q_LEN, int32_t KV_LEN,
+                           int32_t Bq, int32_t Bk) {
+  MaskLayout L;
+  if (mask_layout(rule, B, H, Q_LEN, KV_LEN, Bq, Bk, &L) != FA_OK) return 0;
+  return L.total;
+}
+
+fa_status fa_create_block_mask(const fa_mask_rule* rule, int32_t B, int32_t H, int32_t Q_LEN, int32_t KV_LEN,
+                               int32_t Bq, int32_t Bk, void* dev_buf, size_t buf_bytes, fa_block_mask* out,
+                               fa_stream_t stream) {
+  if (!rule || !out || !dev_buf) return FA_ERR_INVALID_ARG;
+  MaskLayout L;
+  int s = mask_layout(rule, B, H, Q_LEN, KV_LEN, Bq, Bk, &L);
+  if (s != FA_OK) return (fa_status)s;
+  if (buf_bytes < L.total) return FA_ERR_BUFFER_TOO_SMALL;
+  if (reinterpret_cast<uintptr_t>(dev_buf) & 255u) return FA_ERR_INVALID_ARG;
+  DevRule R;
+  s = compile_rule(rule, &R);
+  if (s != FA_OK) return (fa_status)s;
+  // per-batch state (document layouts per b, per-request query offsets) needs a per-batch table
+  const bool per_b_state = (R.any_doc && rule->doc_batch > 1) || rule->q_offset != nullptr;
+  if (per_b_state && !rule->batch_dependent && B > 1) return FA_ERR_INVALID_ARG;
+  if (R.any_doc && (rule->doc_batch != 1 && rule->doc_batch != B)) return FA_ERR_SHAPE;
+  if (R.any_doc && rule->doc_len < KV_LEN) return FA_ERR_SHAPE;
+  uint8_t* base = static_cast<uint8_t*>(dev_buf);
+  MaskOut T;
+  T.Bm = L.Bm;
+  T.Hm = L.Hm;
+  T.q_len = Q_LEN;
+  T.kv_len = KV_LEN;
+  T.bq = Bq;
+  T.bk = Bk;
+  T.nq = L.nq;
+  T.nk = L.nk;
+  T.kv_num = reinterpret_cast<int32_t*>(base + L.off[0]);
+  T.full_kv_num = reinterpret_cast<int32_t*>(base + L.off[1]);
+  T.q_num = reinterpret_cast<int32_t*>(base + L.off[2]);
+  T.full_q_num = reinterpret_cast<int32_t*>(base + L.off[3]);
+  T.kv_idx = reinterpret_cast<int32_t*>(base + L.off[4]);
+  T.full_kv_idx = reinterpret_cast<int32_t*>(base + L.off[5]);
+  T.q_idx = reinterpret_cast<int32_t*>(base + L.off[6]);
+  T.full_q_idx = reinterpret_cast<int32_t*>(base + L.off[7]);
+  T.block_class = base + L.off[8];
+  if (L.Hm > 65535 || L.Bm > 65535 || L.nq > INT_MAX / 2 || L.nk > 65535 * 1024) return FA_ERR_UNSUPPORTED;
+  if (launch_mask_build(R, T, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  out->Bm = T.Bm;
+  out->Hm = T.Hm;
+  out->q_len = Q_LEN;
+  out->kv_len = KV_LEN;
+  out->bq = Bq;
+  out->bk = Bk;
+  out->nq = T.nq;
+  out->nk = T.nk;
+  out->kv_num = T.kv_num;
+  out->kv_idx = T.kv_idx;
+  out->full_kv_num = T.full_kv_num;
+  out->full_kv_idx = T.full_kv_idx;
+  out->q_num = T.q_num;
+  out->q_idx = T.q_idx;
+  out->full_q_num = T.full_q_num;
+  out->full_q_idx = T.full_q_idx;
+  out->block_class = T.block_class;
+  out->rule = *rule;
+  return FA_OK;
+}
+
+fa_status fa_flex_forward(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
+                          const fa_score_rule* score_rule, float scale, void* out, float* lse, int32_t B,
+                          int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d, int32_t* dev_status,
+                          int64_t* dev_counters, fa_stream_t stream) {
+  return (fa_status)forward_impl(false, q, k, v, block_mask, score_rule, scale, out, lse, B, Hq, Hkv, Q_LEN, KV_LEN,
+                                 d, dev_status, dev_counters, stream);
+}
+
+fa_status fa_flex_forward_mma(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
+                              const fa_score_rule* score_rule, float scale, void* out, float* lse, int32_t B,
+                              int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d,
+                              int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream) {
+  return (fa_status)forward_impl(true, q, k, v, block_mask, score_rule, scale, out, lse, B, Hq, Hkv, Q_LEN, KV_LEN,
+                                 d, dev_status, dev_counters, stream);
+}
+
+size_t fa_decode_workspace_bytes(int32_t Bz, int32_t Hq, int32_t d, int32_t max_pages, int32_t page) {
+  if (Bz < 1 || Hq < 1 || d < 1 || max_pages < 1 || page < 1) return 0;
+  const int ps = decode_pages_per_split(page, max_pages);
+  const size_t ns = (size_t)((max_pages + ps - 1) / ps);
+  const size_t slots = (size_t)Bz * Hq * ns;
+  return align256(slots * 4) * 2 + align256(slots * (size_t)d * 4);
+}
+
+fa_status fa_flex_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                         int32_t n_pages_total, const fa_block_mask* bm, const fa_score_rule* score_rule,
+                         float scale, void* out, float* lse, int32_t Bz, int32_t Hq, int32_t Hkv, int32_t d,
+                         int32_t page, int32_t max_pages, void* workspace, size_t workspace_bytes,
+                         int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !page_table || !bm || !out || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  if (Bz < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || n_pages_total < 1 || max_pages < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (page != 32 && page != 64 && page != 128 && page != 256) return FA_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16) return FA_ERR_UNSUPPORTED;
+  if (bm->bq != 1 || bm->bk != page || bm->q_len != 1 || (int64_t)bm->kv_len != (int64_t)max_pages * page ||
+      bm->Hm != 1 || !(bm->Bm == 1 || bm->Bm == Bz) || bm->nk != max_pages || bm->nq != 1)
+    return FA_ERR_SHAPE;
+  if ((int64_t)n_pages_total * Hkv * page > INT_MAX) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(workspace))
+    return FA_ERR_INVALID_ARG;
+  const size_t need = fa_decode_workspace_bytes(Bz, Hq, d, max_pages, page);
+  if (workspace_bytes < need) return FA_ERR_BUFFER_TOO_SMALL;
+  DecArgs a;
+  std::memset(&a, 0, sizeof(a));
+  int s = compile_rule(&bm->rule, &a.rule);
+  if (s != FA_OK) return (fa_status)s;
+  a.q = q;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.page_table = page_table;
+  a.n_pages_total = n_pages_total;
+  a.out = out;
+  a.lse = lse;
+  a.Bz = Bz;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.page = page;
+  a.max_pages = max_pages;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt((float)d);
+  a.score = make_score(score_rule, bm->kv_len);
+  a.mask = dev_mask(bm);
+  a.pages_per_split = decode_pages_per_split(page, max_pages);
+  a.n_splits = (max_pages + a.pages_per_split - 1) / a.pages_per_split;
+  const size_t slots = (size_t)Bz * Hq * a.n_splits;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  a.ws_m = reinterpret_cast<float*>(w);
+  a.ws_l = reinterpret_cast<float*>(w + align256(slots * 4));
+  a.ws_u = reinterpret_cast<float*>(w + 2 * align256(slots * 4));
+  a.status = dev_status;
+  a.counters = dev_counters;
+  a.timeout_ns = g_timeout_ns.load();
+  return (fa_status)launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_block_mask_stats(const fa_block_mask* bm, int64_t* dev_out, fa_stream_t stream) {
+  if (!bm || !dev_out || !bm->kv_num || !bm->full_kv_num) return FA_ERR_INVALID_ARG;
+  MaskOut T;
+  std::memset(&T, 0, sizeof(T));
+  T.Bm = bm->Bm;
+  T.Hm = bm->Hm;
+  T.nq = bm->nq;
+  T.nk = bm->nk;
+  T.kv_num = bm->kv_num;
+  T.full_kv_num = bm->full_kv_num;
+  return launch_mask_stats(T, dev_out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                                : FA_ERR_CUDA;
+}
+
+fa_status fa_check_status(const int32_t* dev_status, fa_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+  if (!dev_status) return FA_OK;
+  int32_t h = 0;
+  if (cudaMemcpyAsync(&h, dev_status, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+  return (fa_status)h;
+}
+
+fa_status fa_debug_wait_timeout(int32_t* dev_status, uint64_t timeout_ns, fa_stream_t stream) {
+  if (!dev_status) return FA_ERR_INVALID_ARG;
+  return launch_debug_wait(dev_status, timeout_ns ? timeout_ns : 1, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+// Internal launch interfaces between the C-ABI layer (fa_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fa_internal.cuh"
+
+namespace fa {
+
+// Table pointers and geometry of a BlockMask, as the kernels read it.
+struct DevMask {
+  int32_t Bm, Hm, q_len, kv_len, bq, bk, nq, nk;
+  const int32_t* kv_num;
+  const int32_t* kv_idx;
+  const int32_t* full_kv_num;
+  const int32_t* full_kv_idx;
+};
+
+struct MaskOut {
+  int32_t Bm, Hm, q_len, kv_len, bq, bk, nq, nk;
+  int32_t* kv_num;
+  int32_t* kv_idx;
+  int32_t* full_kv_num;
+  int32_t* full_kv_idx;
+  int32_t* q_num;
+  int32_t* q_idx;
+  int32_t* full_q_num;
+  int32_t* full_q_idx;
+  uint8_t* block_class;
+};
+
+cudaError_t launch_mask_build(const DevRule& R, const MaskOut& T, cudaStream_t st);
+cudaError_t launch_mask_stats(const MaskOut& T, int64_t* dev_out, cudaStream_t st);
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+  int32_t B, Hq, Hkv, q_len, kv_len, d;
+  float scale;
+  DevRule rule;
+  DevScore score;
+  DevMask mask;
+  int32_t* status;
+  int64_t* counters;
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t st);
+// Returns FA_OK / FA_ERR_UNSUPPORTED / FA_ERR_CUDA.
+int launch_fwd_tc5(const FwdArgs& a, cudaStream_t st);
+
+struct DecArgs {
+  const void* q;
+  const void* k_pages;
+  const void* v_pages;
+  const int32_t* page_table;
+  int32_t n_pages_total;
+  void* out;
+  float* lse;
+  int32_t Bz, Hq, Hkv, d, page, max_pages;
+  float scale;
+  DevRule rule;
+  DevScore score;
+  DevMask mask;
+  float* ws_m;      // [Bz, Hq, n_splits]
+  float* ws_l;      // [Bz, Hq, n_splits]
+  float* ws_u;      // [Bz, Hq, n_splits, d]
+  int32_t pages_per_split, n_splits;
+  int32_t* status;
+  int64_t* counters;
+  uint64_t timeout_ns;
+};
+
+int launch_decode(const DecArgs& a, cudaStream_t st);
+
+cudaError_t launch_debug_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t st);
+
+// Host helper: encode a bf16 tensor map (dims innermost first) with 128-byte swizzle.
+int encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes /* rank-1 entries */, const uint32_t* box);
+
+}  // namespace fa

@@ -1,0 +1,309 @@
+"""Python binding of libfa.so: argument marshalling only. Every step of the computation runs in the
+library's CUDA kernels; PyTorch provides device memory and the current stream.
+
+Names follow the C ABI (include/fa.h): create_block_mask, flex_forward, flex_decode, ...
+The library must have been built (``__graft_entry__.build()`` or ``python -m
+block_sparse_masked_create_gb300.build``); a missing library is an error, never a fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+MAX_OPS = 16
+MAX_TERMS = 8
+
+OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_CHECK, ERR_BUFFER = range(8)
+_OPS = {"true": 0, "causal": 1, "window": 2, "prefix": 3, "doc": 4, "and": 5, "or": 6}
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+class MaskRule(ctypes.Structure):
+    _fields_ = [("n_ops", ctypes.c_int32), ("op", ctypes.c_int32 * MAX_OPS), ("arg", ctypes.c_int64 * MAX_OPS),
+                ("doc_ids", ctypes.c_void_p), ("doc_batch", ctypes.c_int32), ("doc_len", ctypes.c_int32),
+                ("q_offset", ctypes.c_void_p), ("batch_dependent", ctypes.c_int32),
+                ("head_dependent", ctypes.c_int32)]
+
+
+class ScoreRule(ctypes.Structure):
+    _fields_ = [("alibi_slopes", ctypes.c_void_p), ("rel_bias", ctypes.c_void_p), ("softcap", ctypes.c_float)]
+
+
+class BlockMaskC(ctypes.Structure):
+    _fields_ = [("Bm", ctypes.c_int32), ("Hm", ctypes.c_int32), ("q_len", ctypes.c_int32),
+                ("kv_len", ctypes.c_int32), ("bq", ctypes.c_int32), ("bk", ctypes.c_int32),
+                ("nq", ctypes.c_int32), ("nk", ctypes.c_int32),
+                ("kv_num", ctypes.c_void_p), ("kv_idx", ctypes.c_void_p), ("full_kv_num", ctypes.c_void_p),
+                ("full_kv_idx", ctypes.c_void_p), ("q_num", ctypes.c_void_p), ("q_idx", ctypes.c_void_p),
+                ("full_q_num", ctypes.c_void_p), ("full_q_idx", ctypes.c_void_p),
+                ("block_class", ctypes.c_void_p), ("rule", MaskRule)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libfa.so (raises if it has not been built: there is no fallback path)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libfa.so not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    P = ctypes.POINTER
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_status_string.argtypes = [ctypes.c_int]
+    lib.fa_version.restype = ctypes.c_char_p
+    lib.fa_block_mask_bytes.restype = sz
+    lib.fa_block_mask_bytes.argtypes = [P(MaskRule), i32, i32, i32, i32, i32, i32]
+    lib.fa_create_block_mask.restype = ctypes.c_int
+    lib.fa_create_block_mask.argtypes = [P(MaskRule), i32, i32, i32, i32, i32, i32, vp, sz, P(BlockMaskC), vp]
+    fwd_args = [vp, vp, vp, P(BlockMaskC), P(ScoreRule), f32, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.fa_flex_forward.restype = ctypes.c_int
+    lib.fa_flex_forward.argtypes = fwd_args
+    lib.fa_flex_forward_mma.restype = ctypes.c_int
+    lib.fa_flex_forward_mma.argtypes = fwd_args
+    lib.fa_decode_workspace_bytes.restype = sz
+    lib.fa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    lib.fa_flex_decode.restype = ctypes.c_int
+    lib.fa_flex_decode.argtypes = [vp, vp, vp, vp, i32, P(BlockMaskC), P(ScoreRule), f32, vp, vp, i32, i32, i32, i32,
+                                   i32, i32, vp, sz, vp, vp, vp]
+    lib.fa_block_mask_stats.restype = ctypes.c_int
+    lib.fa_block_mask_stats.argtypes = [P(BlockMaskC), vp, vp]
+    lib.fa_check_status.restype = ctypes.c_int
+    lib.fa_check_status.argtypes = [vp, vp]
+    lib.fa_set_wait_timeout_ns.restype = None
+    lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.fa_get_wait_timeout_ns.restype = ctypes.c_uint64
+    lib.fa_get_wait_timeout_ns.argtypes = []
+    lib.fa_debug_wait_timeout.restype = ctypes.c_int
+    lib.fa_debug_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
+    lib.fa_debug_tc5_gemm.restype = ctypes.c_int
+    lib.fa_debug_tc5_gemm.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().fa_status_string(code).decode()
+    except Exception:  # library not loadable
+        return f"status {code}"
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        raise FaError(code, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+# ----------------------------------------------------------------------------------------------
+# rules
+# ----------------------------------------------------------------------------------------------
+def make_mask_rule(spec: Sequence[tuple], doc_ids: Optional[torch.Tensor] = None,
+                   q_offset: Optional[torch.Tensor] = None, batch_dependent: Optional[bool] = None,
+                   head_dependent: bool = False) -> MaskRule:
+    """Rule spec (postfix tuples, see workloads.py) -> fa_mask_rule. doc_ids int32 [doc_batch, doc_len] and
+    q_offset int32 [B] must be device tensors and stay alive while the rule is used."""
+    if not 1 <= len(spec) <= MAX_OPS:
+        raise ValueError("rule must have 1..16 ops")
+    r = MaskRule()
+    r.n_ops = len(spec)
+    for i, op in enumerate(spec):
+        r.op[i] = _OPS[op[0]]
+        r.arg[i] = int(op[1]) if len(op) > 1 else 0
+    if doc_ids is not None:
+        if doc_ids.dtype != torch.int32 or doc_ids.dim() != 2 or not doc_ids.is_contiguous():
+            raise ValueError("doc_ids must be contiguous int32 [doc_batch, doc_len]")
+        r.doc_ids = doc_ids.data_ptr()
+        r.doc_batch, r.doc_len = doc_ids.shape
+    if q_offset is not None:
+        if q_offset.dtype != torch.int32 or not q_offset.is_contiguous():
+            raise ValueError("q_offset must be contiguous int32 [B]")
+        r.q_offset = q_offset.data_ptr()
+    if batch_dependent is None:
+        batch_dependent = q_offset is not None or (doc_ids is not None and doc_ids.shape[0] > 1)
+    r.batch_dependent = int(bool(batch_dependent))
+    r.head_dependent = int(bool(head_dependent))
+    return r
+
+
+def make_score_rule(alibi_slopes: Optional[torch.Tensor] = None, rel_bias: Optional[torch.Tensor] = None,
+                    softcap: float = 0.0) -> ScoreRule:
+    s = ScoreRule()
+    for t in (alibi_slopes, rel_bias):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError("score tables must be contiguous fp32 device tensors")
+    s.alibi_slopes = None if alibi_slopes is None else alibi_slopes.data_ptr()
+    s.rel_bias = None if rel_bias is None else rel_bias.data_ptr()
+    s.softcap = float(softcap or 0.0)
+    return s
+
+
+# ----------------------------------------------------------------------------------------------
+# BlockMask
+# ----------------------------------------------------------------------------------------------
+@dataclass
+class BlockMask:
+    c: BlockMaskC
+    buf: torch.Tensor
+    keep: list = field(default_factory=list)   # tensors the rule points into
+
+    @property
+    def shape(self):
+        return (self.c.Bm, self.c.Hm, self.c.nq, self.c.nk)
+
+    def _view(self, addr: int, n: int, dtype) -> torch.Tensor:
+        off = addr - self.buf.data_ptr()
+        nbytes = n * (4 if dtype == torch.int32 else 1)
+        return self.buf[off:off + nbytes].view(dtype)
+
+    def tables(self) -> dict:
+        """Device views of the tables: kv_num [Bm,Hm,nq], kv_idx [Bm,Hm,nq,nk], ..., block_class."""
+        Bm, Hm, nq, nk = self.shape
+        c = self.c
+        out = {}
+        for name, n, shp in (("kv_num", Bm * Hm * nq, (Bm, Hm, nq)), ("full_kv_num", Bm * Hm * nq, (Bm, Hm, nq)),
+                             ("q_num", Bm * Hm * nk, (Bm, Hm, nk)), ("full_q_num", Bm * Hm * nk, (Bm, Hm, nk)),
+                             ("kv_idx", Bm * Hm * nq * nk, (Bm, Hm, nq, nk)),
+                             ("full_kv_idx", Bm * Hm * nq * nk, (Bm, Hm, nq, nk)),
+                             ("q_idx", Bm * Hm * nk * nq, (Bm, Hm, nk, nq)),
+                             ("full_q_idx", Bm * Hm * nk * nq, (Bm, Hm, nk, nq))):
+            out[name] = self._view(getattr(c, name), n, torch.int32).view(shp)
+        out["block_class"] = self._view(c.block_class, Bm * Hm * nq * nk, torch.uint8).view(Bm, Hm, nq, nk)
+        return out
+
+
+def block_mask_bytes(rule: MaskRule, B: int, H: int, Q_LEN: int, KV_LEN: int, Bq: int, Bk: int) -> int:
+    return int(load().fa_block_mask_bytes(ctypes.byref(rule), B, H, Q_LEN, KV_LEN, Bq, Bk))
+
+
+def create_block_mask(rule: MaskRule, B: int, H: int, Q_LEN: int, KV_LEN: int, Bq: int = 128, Bk: int = 128,
+                      device="cuda", keep: Optional[list] = None, buf: Optional[torch.Tensor] = None) -> BlockMask:
+    """fa_create_block_mask: classify every block, compact the lists, build the transpose (on `device`)."""
+    lib = load()
+    n = block_mask_bytes(rule, B, H, Q_LEN, KV_LEN, Bq, Bk)
+    if n == 0:
+        raise FaError(ERR_SHAPE, "fa_block_mask_bytes")
+    if buf is None or buf.numel() < n:
+        buf = torch.empty(n, dtype=torch.uint8, device=device)
+    c = BlockMaskC()
+    _check(lib.fa_create_block_mask(ctypes.byref(rule), B, H, Q_LEN, KV_LEN, Bq, Bk, _ptr(buf), buf.numel(),
+                                    ctypes.byref(c), _stream(buf.device)), "fa_create_block_mask")
+    return BlockMask(c, buf, list(keep or []))
+
+
+def recreate_block_mask(bm: BlockMask, rule: MaskRule, B: int, H: int, Q_LEN: int, KV_LEN: int, Bq: int,
+                        Bk: int) -> None:
+    """Rebuild into an existing BlockMask's buffer (same sizes; no allocation)."""
+    _check(load().fa_create_block_mask(ctypes.byref(rule), B, H, Q_LEN, KV_LEN, Bq, Bk, _ptr(bm.buf), bm.buf.numel(),
+                                       ctypes.byref(bm.c), _stream(bm.buf.device)), "fa_create_block_mask")
+
+
+def block_mask_stats(bm: BlockMask, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """int64[6] on the device: full, partial, empty, max row length, sum of row lengths, rows."""
+    if out is None:
+        out = torch.empty(6, dtype=torch.int64, device=bm.buf.device)
+    _check(load().fa_block_mask_stats(ctypes.byref(bm.c), _ptr(out), _stream(out.device)), "fa_block_mask_stats")
+    return out
+
+
+# ----------------------------------------------------------------------------------------------
+# attention
+# ----------------------------------------------------------------------------------------------
+def flex_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: BlockMask,
+                 score: Optional[ScoreRule] = None, scale: Optional[float] = None,
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 status: Optional[torch.Tensor] = None, counters: Optional[torch.Tensor] = None,
+                 force_mma: bool = False):
+    """fa_flex_forward: q [B,Hq,Q_LEN,d], k/v [B,Hkv,KV_LEN,d] bf16 contiguous on the GPU.
+    Returns (out bf16 [B,Hq,Q_LEN,d], lse fp32 [B,Hq,Q_LEN])."""
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    B, Hq, Q_LEN, d = q.shape
+    Hkv, KV_LEN = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Q_LEN), dtype=torch.float32, device=q.device)
+    fn = load().fa_flex_forward_mma if force_mma else load().fa_flex_forward
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(block_mask.c), ctypes.byref(score) if score else None,
+              float(scale) if scale else 0.0, _ptr(out), _ptr(lse), B, Hq, Hkv, Q_LEN, KV_LEN, d, _ptr(status),
+              _ptr(counters), _stream(q.device)), "fa_flex_forward")
+    return out, lse
+
+
+def decode_workspace_bytes(Bz: int, Hq: int, d: int, max_pages: int, page: int) -> int:
+    return int(load().fa_decode_workspace_bytes(Bz, Hq, d, max_pages, page))
+
+
+def flex_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, page_table: torch.Tensor,
+                block_mask: BlockMask, score: Optional[ScoreRule] = None, scale: Optional[float] = None,
+                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                counters: Optional[torch.Tensor] = None):
+    """fa_flex_decode: q [Bz,Hq,d], k/v pages [P,Hkv,page,d] bf16, page_table int32 [Bz,max_pages]."""
+    Bz, Hq, d = q.shape
+    P, Hkv, page, _ = k_pages.shape
+    max_pages = page_table.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Bz, Hq), dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes(Bz, Hq, d, max_pages, page)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(load().fa_flex_decode(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), P,
+                                 ctypes.byref(block_mask.c), ctypes.byref(score) if score else None,
+                                 float(scale) if scale else 0.0, _ptr(out), _ptr(lse), Bz, Hq, Hkv, d, page, max_pages,
+                                 _ptr(workspace), workspace.numel(), _ptr(status), _ptr(counters),
+                                 _stream(q.device)), "fa_flex_decode")
+    return out, lse
+
+
+def check_status(status: torch.Tensor) -> int:
+    return int(load().fa_check_status(_ptr(status), _stream(status.device)))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    load().fa_set_wait_timeout_ns(int(ns))
+
+
+def get_wait_timeout_ns() -> int:
+    return int(load().fa_get_wait_timeout_ns())
+
+
+def debug_wait_timeout(status: torch.Tensor, timeout_ns: int) -> int:
+    return int(load().fa_debug_wait_timeout(_ptr(status), int(timeout_ns), _stream(status.device)))
+
+
+def debug_tc5_gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, K: int, b_mn_major: bool, use_tma: bool,
+                   status: Optional[torch.Tensor] = None) -> int:
+    return int(load().fa_debug_tc5_gemm(_ptr(A), _ptr(B), _ptr(C), K, int(b_mn_major), int(use_tma), _ptr(status),
+                                        _stream(A.device)))

@@ -1,0 +1,233 @@
+/*
+ * fa.h -- C ABI of libfa.so: masked attention over a block-sparse BlockMask on GB300 (sm_103a).
+ *
+ * Three operations, as described on the pages this library implements:
+ *   fa_create_block_mask  -- evaluate a mask rule tile by tile and emit the BlockMask tables
+ *                            ("5.1.2 FlexAttention: from rules to fused kernels", sections 2.1-2.2;
+ *                             "FlexAttention: compiler optimisation of custom attention", section 4).
+ *   fa_flex_forward       -- FlashAttention-style forward that visits only the non-empty KV blocks of each
+ *                            query block, applies the score rule, masks partial blocks only, and writes O
+ *                            and LSE ("5.1.2 FlexAttention ...", section 3.1; "FlexAttention: compiler
+ *                            optimisation ...", section 3).
+ *   fa_flex_decode        -- one new query token per request over a paged KV cache, split along KV and
+ *                            merged by the online-softmax law ("5.1.2 FlexAttention ...", sections 3.2 and
+ *                            5; "FlexAttention: compiler optimisation ...", section 6; "5 Kernels: turning
+ *                            logical sparsity into real speed-ups", section 3).
+ *
+ * Conventions shared by every entry point
+ *  - Memory: the caller owns all memory. Pointers marked "device" must be device pointers of the current
+ *    CUDA device; "host" pointers are read during the call only. The library keeps no state between
+ *    calls and allocates no device memory.
+ *  - Streams: all device work is enqueued on `stream` (NULL = legacy default stream). No entry point
+ *    synchronises except fa_check_status.
+ *  - Argument errors are detected on the host before anything is launched and return FA_ERR_* without
+ *    side effects. Errors only the device can see (an out-of-range page id, a pipeline wait that timed
+ *    out) are written to *dev_status (first error wins) and read back with fa_check_status.
+ *  - Layouts are row-major and contiguous unless stated. bf16 = IEEE bfloat16 bit patterns (uint16).
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,     /* NULL where a pointer is required, malformed rule, bad enum */
+  FA_ERR_SHAPE = 2,           /* sizes inconsistent with each other or with the BlockMask */
+  FA_ERR_UNSUPPORTED = 3,     /* valid but not implemented (head dim, block size, GQA group > 16) */
+  FA_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed (launch, copy, tensor-map encode) */
+  FA_ERR_TIMEOUT = 5,         /* device: a bounded pipeline wait gave up (the kernel returned early) */
+  FA_ERR_DEVICE_CHECK = 6,    /* device: an index read from memory was out of range (e.g. a page id) */
+  FA_ERR_BUFFER_TOO_SMALL = 7 /* caller-provided buffer/workspace smaller than required */
+} fa_status;
+
+FA_API const char* fa_status_string(fa_status s);
+
+/* ------------------------------------------------------------------------------------------------
+ * Mask rule (mask_mod): a postfix program over (b, h, q_idx, kv_idx) -> allowed.
+ * "5.1.2 FlexAttention ...", section 1.1 (causal i >= j, left window i - j < W, document equality,
+ * and_masks / or_masks); prefix-LM j < P OR causal as in the causal-pruning article, section 5.
+ * i is the GLOBAL query position i = q_idx + q_offset[b] ("FlexAttention: compiler optimisation ...",
+ * section 6: a decode query at position t must be compared as t, not 0).
+ * Atoms push one value, FA_M_AND / FA_M_OR pop two and push one; exactly one value must remain.
+ * The library rewrites the program into at most FA_MAX_RULE_TERMS OR-ed conjunctions; larger
+ * expansions return FA_ERR_UNSUPPORTED.
+ * ---------------------------------------------------------------------------------------------- */
+#define FA_MAX_RULE_OPS 16
+#define FA_MAX_RULE_TERMS 8
+
+typedef enum {
+  FA_M_TRUE = 0,   /* every pair */
+  FA_M_CAUSAL = 1, /* kv_idx <= i */
+  FA_M_WINDOW = 2, /* i - kv_idx < arg  (arg = W >= 1; the window includes the current token) */
+  FA_M_PREFIX = 3, /* kv_idx < arg      (arg = P >= 0) */
+  FA_M_DOC = 4,    /* doc_ids[b][i] == doc_ids[b][kv_idx] */
+  FA_M_AND = 5,
+  FA_M_OR = 6
+} fa_mask_op;
+
+typedef struct {
+  int32_t n_ops;                   /* 1..FA_MAX_RULE_OPS */
+  int32_t op[FA_MAX_RULE_OPS];     /* fa_mask_op */
+  int64_t arg[FA_MAX_RULE_OPS];    /* W for FA_M_WINDOW, P for FA_M_PREFIX, ignored otherwise */
+  const int32_t* doc_ids;          /* device int32 [doc_batch, doc_len]; required iff a FA_M_DOC op */
+  int32_t doc_batch;               /* 1 (one sequence layout for all b) or B */
+  int32_t doc_len;                 /* must cover every global position read on both sides */
+  const int32_t* q_offset;         /* device int32 [B] or NULL (= all zero) */
+  int32_t batch_dependent;         /* 0: table broadcast over b (Bm = 1); 1: Bm = B */
+  int32_t head_dependent;          /* 0: table broadcast over h (Hm = 1); 1: Hm = H */
+} fa_mask_rule;
+
+/* ------------------------------------------------------------------------------------------------
+ * Score rule (score_mod), applied to the already-scaled score s = scale * <q_i, k_j> in the fixed
+ * order  s -> s + alibi -> + rel_bias -> softcap  (the c(a*s + r) order; "5.1.2 FlexAttention ...",
+ * section 1.2). Every absent part is the identity. Head index = the QUERY head (GQA: section 1.2).
+ * ---------------------------------------------------------------------------------------------- */
+typedef struct {
+  const float* alibi_slopes; /* device fp32 [Hq] or NULL:  s += -slope[h] * (i - j) */
+  const float* rel_bias;     /* device fp32 [Hq, 2*KV_LEN-1] or NULL:  s += rel_bias[h][(i - j) + KV_LEN - 1] */
+  float softcap;             /* > 0: s = softcap * tanh(s / softcap);  <= 0: off */
+} fa_score_rule;
+
+/* ------------------------------------------------------------------------------------------------
+ * BlockMask ("5.1.2 FlexAttention ...", sections 2.1-2.2; "5 Kernels ...", section 4): per query block
+ * row r (Bq rows) the partial KV blocks (kv_num / kv_idx) and the full ones (full_kv_num / full_kv_idx),
+ * column ids ascending, unused slots 0; the query-side transpose per KV block c (q_num / q_idx,
+ * full_q_num / full_q_idx), row ids ascending, unused slots 0. A block is full when every pair of its
+ * Bq x Bk footprint is allowed, empty when none is, partial otherwise; pairs outside [0,Q_LEN) x
+ * [0,KV_LEN) count as not allowed, so a ragged tail block is at most partial.
+ * All arrays point into the caller's buffer given to fa_create_block_mask. The rule is kept by value
+ * (its device pointers must stay valid while the mask is used).
+ * ---------------------------------------------------------------------------------------------- */
+typedef struct {
+  int32_t Bm, Hm, q_len, kv_len, bq, bk, nq, nk;
+  int32_t* kv_num;          /* [Bm,Hm,nq]    */
+  int32_t* kv_idx;          /* [Bm,Hm,nq,nk] */
+  int32_t* full_kv_num;     /* [Bm,Hm,nq]    */
+  int32_t* full_kv_idx;     /* [Bm,Hm,nq,nk] */
+  int32_t* q_num;           /* [Bm,Hm,nk]    */
+  int32_t* q_idx;           /* [Bm,Hm,nk,nq] */
+  int32_t* full_q_num;      /* [Bm,Hm,nk]    */
+  int32_t* full_q_idx;      /* [Bm,Hm,nk,nq] */
+  uint8_t* block_class;     /* [Bm,Hm,nq,nk]: 0 empty, 1 partial, 2 full */
+  fa_mask_rule rule;
+} fa_block_mask;
+
+/* Bytes of device buffer fa_create_block_mask needs for these sizes (0 on invalid arguments). */
+FA_API size_t fa_block_mask_bytes(const fa_mask_rule* rule, int32_t B, int32_t H, int32_t Q_LEN, int32_t KV_LEN,
+                           int32_t Bq, int32_t Bk);
+
+/* create_block_mask(mask_mod, B, H, Q_LEN, KV_LEN, BLOCK_SIZE) ("FlexAttention: compiler optimisation
+ * ...", section 5; "5.1.2 FlexAttention ...", section 2.2 "building the table from mask_mod"):
+ * classify every (b_m, h_m, r, c) block by evaluating the rule over its footprint, compact the partial
+ * and full lists, and build the query-side transpose.
+ *   rule      host pointer, copied into *out
+ *   B, H      batch and query-head counts the mask is used with (Bm = B or 1, Hm = H or 1 per the rule)
+ *   Bq, Bk    block sizes, 1..128 each
+ *   dev_buf   device buffer of >= fa_block_mask_bytes(...) bytes, 256-byte aligned
+ *   out       host struct, filled with pointers into dev_buf
+ * Returns FA_ERR_BUFFER_TOO_SMALL, FA_ERR_SHAPE (non-positive sizes, Bq/Bk out of range, doc ids too
+ * short), FA_ERR_INVALID_ARG (malformed rule, a rule that reads per-batch state with
+ * batch_dependent = 0), FA_ERR_UNSUPPORTED (rule expands to more than FA_MAX_RULE_TERMS terms). */
+FA_API fa_status fa_create_block_mask(const fa_mask_rule* rule, int32_t B, int32_t H, int32_t Q_LEN, int32_t KV_LEN,
+                               int32_t Bq, int32_t Bk, void* dev_buf, size_t buf_bytes, fa_block_mask* out,
+                               fa_stream_t stream);
+
+/* flex_attention(q, k, v, score_mod, block_mask, scale) forward ("5.1.2 FlexAttention ...", section
+ * 3.1: for each query block visit the full list without the mask and the partial list with it, keep the
+ * online-softmax state (m, l, acc), write O = acc / l and LSE = m + ln l; an empty row writes O = 0,
+ * LSE = -inf).
+ *   q            device bf16 [B, Hq, Q_LEN, d]
+ *   k, v         device bf16 [B, Hkv, KV_LEN, d]; query head h reads KV head floor(h / (Hq/Hkv))
+ *   block_mask   host pointer to a mask made by fa_create_block_mask with q_len == Q_LEN, kv_len ==
+ *                KV_LEN, Bm in {1, B}, Hm in {1, Hq} (a length mismatch is an error, never trimmed)
+ *   score_rule   host pointer or NULL (no score rule)
+ *   scale        > 0, or <= 0 for 1/sqrt(d)
+ *   out          device bf16 [B, Hq, Q_LEN, d];   lse  device fp32 [B, Hq, Q_LEN] (natural log)
+ *   dev_status   device int32 or NULL (device-side errors are then not reported)
+ *   dev_counters device int64[4] or NULL: += {query tiles, full blocks visited, partial blocks visited,
+ *                K/V tile loads issued} (for checking that empty blocks issue no loads)
+ * Supported: d in {64, 128}; Bq, Bk in {16, 32, 64, 128}; Q_LEN, KV_LEN >= 1; Hq % Hkv == 0;
+ * q/k/v/out 16-byte aligned. Bq == Bk == 128 runs the tcgen05/TMEM kernel, other block sizes the
+ * mma.sync kernel. */
+FA_API fa_status fa_flex_forward(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
+                          const fa_score_rule* score_rule, float scale, void* out, float* lse,
+                          int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d,
+                          int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream);
+
+/* Same as fa_flex_forward but always uses the mma.sync kernel (a second, independent kernel over the
+ * same tables; used to cross-check the tcgen05 path). */
+FA_API fa_status fa_flex_forward_mma(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
+                              const fa_score_rule* score_rule, float scale, void* out, float* lse,
+                              int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d,
+                              int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream);
+
+/* Paged split-KV decode ("5.1.2 FlexAttention ...", sections 3.2 "split-KV exact merge" and 5.1-5.2;
+ * "FlexAttention: compiler optimisation ...", section 6; the merge law of "5 Kernels ...", section 3).
+ * One query token per request. Logical KV block c of request b lives in physical page
+ * page_table[b][c]; rules use logical positions. Each (request, KV head, split) program reads every K/V
+ * byte of its pages once for all Hq/Hkv query heads, keeps (m, l, u) for its pages, and a second kernel
+ * merges the splits: m = max m_s, l = sum e^(m_s - m) l_s, O = sum e^(m_s - m) u_s / l.
+ *   q            device bf16 [Bz, Hq, d]
+ *   k_pages,
+ *   v_pages      device bf16 [n_pages_total, Hkv, page, d]
+ *   page_table   device int32 [Bz, max_pages]
+ *   block_mask   made with Bq = 1, Bk = page, Q_LEN = 1, KV_LEN = max_pages * page, Bm in {1, Bz},
+ *                Hm == 1; its rule's q_offset[b] is the query's global position (cur_pos = L_b - 1)
+ *   workspace    device buffer of >= fa_decode_workspace_bytes(...) bytes, 16-byte aligned
+ *   out          device bf16 [Bz, Hq, d];  lse  device fp32 [Bz, Hq]
+ * Supported: d in {64, 128}; page in {32, 64, 128, 256}; 1 <= Hq/Hkv <= 16.
+ * A page id outside [0, n_pages_total) sets FA_ERR_DEVICE_CHECK in *dev_status (that page is skipped). */
+FA_API size_t fa_decode_workspace_bytes(int32_t Bz, int32_t Hq, int32_t d, int32_t max_pages, int32_t page);
+FA_API fa_status fa_flex_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                         int32_t n_pages_total, const fa_block_mask* block_mask, const fa_score_rule* score_rule,
+                         float scale, void* out, float* lse, int32_t Bz, int32_t Hq, int32_t Hkv, int32_t d,
+                         int32_t page, int32_t max_pages, void* workspace, size_t workspace_bytes,
+                         int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream);
+
+/* Block statistics of a BlockMask ("5.1.2 FlexAttention ...", sections 2.2 and 6.3: full/partial/empty
+ * counts and row lengths). dev_out: device int64[6] = {full, partial, empty, max row length (full +
+ * partial), sum of row lengths, rows}. Enqueued on stream, no synchronisation. */
+FA_API fa_status fa_block_mask_stats(const fa_block_mask* block_mask, int64_t* dev_out, fa_stream_t stream);
+
+/* Synchronise `stream`, read *dev_status and return it as an fa_status (FA_ERR_CUDA if the stream
+ * reported a CUDA error). Does not clear *dev_status. */
+FA_API fa_status fa_check_status(const int32_t* dev_status, fa_stream_t stream);
+
+/* Bounded waits. Every pipeline wait inside the kernels gives up after this many nanoseconds, sets
+ * FA_ERR_TIMEOUT and returns. Default 2e9 (2 s). Process-wide setting read at launch time. */
+FA_API void fa_set_wait_timeout_ns(uint64_t ns);
+FA_API uint64_t fa_get_wait_timeout_ns(void);
+
+/* Self-test of the bounded wait: launches one CTA that waits on an mbarrier nothing ever arrives on,
+ * with a limit of timeout_ns; the kernel must return and set FA_ERR_TIMEOUT in *dev_status. */
+FA_API fa_status fa_debug_wait_timeout(int32_t* dev_status, uint64_t timeout_ns, fa_stream_t stream);
+
+/* Self-test of one tcgen05 MMA chain (128 x 128 x K, bf16 in, fp32 accumulate in tensor memory):
+ * C = A * B^T with A device bf16 [128, K] and B device bf16 [128, K] (b_mn_major = 0, B K-major), or
+ * C = A * B with B device bf16 [K, 128] (b_mn_major = 1, B MN-major); C device fp32 [128, 128].
+ * K in {64, 128}. use_tma = 1 stages the tiles with TMA (128-byte swizzle), 0 with plain stores in the
+ * same swizzled layout. Used by the tests to pin the shared-memory and instruction descriptors. */
+FA_API fa_status fa_debug_tc5_gemm(const void* A, const void* B, float* C, int32_t K, int32_t b_mn_major,
+                            int32_t use_tma, int32_t* dev_status, fa_stream_t stream);
+
+/* Library version string. */
+FA_API const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_H_ */

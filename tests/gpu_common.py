@@ -1,0 +1,119 @@
+"""Shared helpers of the GPU parity tests: run the library through the C ABI on seeded inputs and compare
+with the fp64 oracle on the same inputs (full tensors for small cases, sampled rows at full size)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from block_sparse_masked_create_gb300 import fa, synth, workloads
+from oracle import flexmask_oracle as orc
+
+# bf16 inputs, fp32 accumulation, fp64 reference (tolerances fixed by the target specification)
+O_MAX, O_MEAN, LSE_MAX = 8e-3, 1e-3, 2e-3
+
+
+def rule_arrays(w: workloads.Prefill, device="cuda"):
+    doc = None if w.doc_ids is None else torch.from_numpy(np.ascontiguousarray(w.doc_ids.astype(np.int32))).to(device)
+    return doc
+
+
+def score_tensors(score: dict, device="cuda"):
+    al = score.get("alibi_slopes")
+    rb = score.get("rel_bias")
+    al_t = None if al is None else torch.tensor(np.asarray(al, dtype=np.float32), device=device)
+    rb_t = None if rb is None else torch.from_numpy(np.ascontiguousarray(np.asarray(rb, dtype=np.float32))).to(device)
+    return al_t, rb_t, fa.make_score_rule(al_t, rb_t, score.get("softcap", 0.0))
+
+
+def oracle_score(score: dict) -> dict:
+    out = {}
+    if score.get("alibi_slopes") is not None:
+        out["alibi_slopes"] = np.asarray(score["alibi_slopes"], dtype=np.float32).astype(np.float64)
+    if score.get("rel_bias") is not None:
+        out["rel_bias"] = np.asarray(score["rel_bias"], dtype=np.float32).astype(np.float64)
+    if score.get("softcap"):
+        out["softcap"] = float(score["softcap"])
+    return out
+
+
+def run_prefill(w: workloads.Prefill, force_mma=False, counters=False, bq=None, bk=None):
+    """Generate (if needed) and run create_block_mask + flex_forward; returns dict of results."""
+    if w.q_bits is None:
+        w.generate()
+    dev = "cuda"
+    q = workloads.bf16_torch(w.q_bits, dev)
+    k = workloads.bf16_torch(w.k_bits, dev)
+    v = workloads.bf16_torch(w.v_bits, dev)
+    doc = rule_arrays(w, dev)
+    rule = fa.make_mask_rule(w.rule, doc_ids=doc)
+    bm = fa.create_block_mask(rule, w.B, w.Hq, w.q_len, w.kv_len, bq or w.bq, bk or w.bk, device=dev, keep=[doc])
+    al, rb, sc = score_tensors(w.score, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(4, dtype=torch.int64, device=dev) if counters else None
+    out, lse = fa.flex_forward(q, k, v, bm, sc, w.scale, status=status, counters=cnt, force_mma=force_mma)
+    st = fa.check_status(status)
+    return dict(out=out, lse=lse, bm=bm, status=st, counters=cnt, keep=(al, rb, doc, q, k, v))
+
+
+def sample_rows(w: workloads.Prefill, n_heads=3, rows_per_block=4, n_blocks=6, seed=0):
+    """Seeded sample: a few (b, h) pairs (first, last, random) and query rows from the first, the last and
+    random query blocks (always including each sampled block's first and last row)."""
+    rng = np.random.default_rng(seed)
+    pairs = {(0, 0), (w.B - 1, w.Hq - 1)}
+    while len(pairs) < min(n_heads, w.B * w.Hq):
+        pairs.add((int(rng.integers(w.B)), int(rng.integers(w.Hq))))
+    nq = -(-w.q_len // w.bq)
+    blocks = {0, nq - 1}
+    while len(blocks) < min(n_blocks, nq):
+        blocks.add(int(rng.integers(nq)))
+    rows = set()
+    for r in blocks:
+        lo, hi = r * w.bq, min(w.q_len, (r + 1) * w.bq)
+        rows.update({lo, hi - 1})
+        rows.update(int(x) for x in rng.integers(lo, hi, size=rows_per_block))
+    return sorted(pairs), np.array(sorted(rows), dtype=np.int64)
+
+
+def oracle_rows(w: workloads.Prefill, pairs, rows):
+    """fp64 oracle O/LSE for the sampled (b, h) pairs and query rows."""
+    g = w.Hq // w.Hkv
+    res = {}
+    for b, h in pairs:
+        hk = h // g
+        qf = synth.bf16_bits_to_f64(w.q_bits[b, h, rows])
+        kf = synth.bf16_bits_to_f64(w.k_bits[b, hk])
+        vf = synth.bf16_bits_to_f64(w.v_bits[b, hk])
+        res[(b, h)] = orc.attention_rows(qf, kf, vf, w.rule, rows, b, h, w.q_len, w.kv_len, w.scale,
+                                         oracle_score(w.score), 0, w.doc_ids)
+    return res
+
+
+def compare(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray, what=""):
+    """Tolerance check: max/mean |O - O*| and max |LSE - LSE*| (empty rows: LSE both -inf, O both 0)."""
+    err = np.abs(o_gpu.astype(np.float64) - o_ref)
+    inf_ref = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lse_gpu), inf_ref), f"{what}: empty-row pattern differs"
+    lerr = np.abs(lse_gpu[~inf_ref].astype(np.float64) - lse_ref[~inf_ref]) if (~inf_ref).any() else np.zeros(1)
+    assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite output"
+    assert err.max() <= O_MAX, f"{what}: max |O err| {err.max():.3e}"
+    assert err.mean() <= O_MEAN, f"{what}: mean |O err| {err.mean():.3e}"
+    assert lerr.max() <= LSE_MAX, f"{what}: max |LSE err| {lerr.max():.3e}"
+    return float(err.max()), float(err.mean()), float(lerr.max())
+
+
+def tables_np(bm: fa.BlockMask) -> dict:
+    t = bm.tables()
+    return {k: v.cpu().numpy() for k, v in t.items()}
+
+
+def assert_tables_equal(got: dict, want: dict, rows=None):
+    keys = ["kv_num", "kv_idx", "full_kv_num", "full_kv_idx", "block_class"]
+    for k in keys:
+        g, w_ = got[k], want[k]
+        if rows is not None:
+            g, w_ = g[:, :, rows], w_[:, :, rows]
+        assert g.shape == w_.shape, f"{k}: shape {g.shape} vs {w_.shape}"
+        assert np.array_equal(g, w_), f"{k}: tables differ"
+    if rows is None:
+        for k in ["q_num", "q_idx", "full_q_num", "full_q_idx"]:
+            assert np.array_equal(got[k], want[k]), f"{k}: tables differ"

@@ -1,0 +1,134 @@
+"""fa_create_block_mask on the GPU vs the oracle: every table bit-exact (counts, ascending ids, zero fill,
+the query-side transpose and the class matrix), on the pages' worked examples, a sweep of rules with
+ragged tails and small blocks, broadcast variants, and the five workloads at full size."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_masked_create_gb300 import fa, workloads
+from oracle import flexmask_oracle as orc
+from tests.gpu_common import assert_tables_equal, tables_np
+
+pytestmark = pytest.mark.gpu
+
+CW = lambda w: [("causal",), ("window", w), ("and",)]
+
+
+def gpu_tables(spec, B, H, q_len, kv_len, bq, bk, doc=None, q_off=None, bdep=None, hdep=False):
+    doc_t = None if doc is None else torch.from_numpy(np.ascontiguousarray(doc, dtype=np.int32)).cuda()
+    off_t = None if q_off is None else torch.from_numpy(np.ascontiguousarray(q_off, dtype=np.int32)).cuda()
+    rule = fa.make_mask_rule(spec, doc_ids=doc_t, q_offset=off_t, batch_dependent=bdep, head_dependent=hdep)
+    bm = fa.create_block_mask(rule, B, H, q_len, kv_len, bq, bk, keep=[doc_t, off_t])
+    torch.cuda.synchronize()
+    return bm, tables_np(bm)
+
+
+def test_worked_example_n8_w4(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "n8_w4_2x2.json")))
+    bm, t = gpu_tables(CW(4), 1, 1, 8, 8, 2, 2)
+    want = orc.block_mask(CW(4), 1, 1, 8, 8, 2, 2)
+    assert_tables_equal(t, want)
+    h = g["hand_derived_tables"]
+    assert t["kv_num"][0, 0].tolist() == h["kv_num"] and t["full_kv_num"][0, 0].tolist() == h["full_kv_num"]
+    assert t["q_num"][0, 0].tolist() == h["q_num"] and t["full_q_num"][0, 0].tolist() == h["full_q_num"]
+    st = fa.block_mask_stats(bm).cpu().tolist()
+    assert st[:3] == [3, 6, 7]                      # full, partial, empty: 9 executed blocks, 7 empty
+
+
+def test_worked_example_n16_w8(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "n16_w8_4x4.json")))
+    _, t = gpu_tables(CW(8), 1, 1, 16, 16, 4, 4)
+    names = {0: "empty", 1: "partial", 2: "full"}
+    assert [names[int(x)] for x in t["block_class"][0, 0, -1]] == g["last_row_classes_by_kv_block"]
+    assert_tables_equal(t, orc.block_mask(CW(8), 1, 1, 16, 16, 4, 4))
+
+
+RULES = [
+    [("causal",)], CW(5), CW(1), [("true",)], [("prefix", 0)],
+    [("causal",), ("prefix", 7), ("or",)],
+    [("window", 6), ("prefix", 3), ("or",)],
+    [("causal",), ("doc",), ("and",)],
+    [("causal",), ("prefix", 9), ("or",), ("doc",), ("and",)],
+    [("doc",), ("window", 4), ("and",), ("prefix", 2), ("or",)],
+]
+
+
+@pytest.mark.parametrize("ri", range(len(RULES)))
+@pytest.mark.parametrize("q_len,kv_len,bq,bk", [(37, 37, 8, 8), (100, 61, 16, 32), (1, 5, 4, 4), (130, 130, 128, 128),
+                                                 (77, 200, 3, 7), (256, 256, 64, 128), (300, 300, 128, 16)])
+def test_rule_sweep_ragged(ri, q_len, kv_len, bq, bk):
+    spec = RULES[ri]
+    n = max(q_len, kv_len)
+    lens = np.array([5, 9, 1, 12, 7, 6, 30, 2, 50, 3, 80, 100, 100])
+    doc = np.repeat(np.arange(len(lens), dtype=np.int32), lens)[:n]
+    doc = np.concatenate([doc, np.full(n - len(doc), 99, np.int32)])[None, :] if len(doc) < n else doc[None, :]
+    uses_doc = any(op[0] == "doc" for op in spec)
+    _, t = gpu_tables(spec, 1, 1, q_len, kv_len, bq, bk, doc=doc if uses_doc else None)
+    want = orc.block_mask(spec, 1, 1, q_len, kv_len, bq, bk, doc_ids=doc if uses_doc else None)
+    assert_tables_equal(t, want)
+
+
+def test_batch_dependent_offsets_and_docs():
+    B, H = 3, 2
+    off = np.array([0, 17, 40], dtype=np.int32)
+    rng = np.random.default_rng(5)
+    doc = np.stack([np.sort(rng.integers(0, 4, size=64)).astype(np.int32) for _ in range(B)])
+    spec = [("causal",), ("doc",), ("and",)]
+    _, t = gpu_tables(spec, B, H, 20, 64, 4, 8, doc=doc, q_off=off, bdep=True)
+    want = orc.block_mask(spec, B, H, 20, 64, 4, 8, batch_dependent=True, q_offset=off, doc_ids=doc)
+    assert_tables_equal(t, want)
+    _, th = gpu_tables([("causal",)], 1, 3, 24, 24, 8, 8, hdep=True)
+    assert_tables_equal(th, orc.block_mask([("causal",)], 1, 3, 24, 24, 8, 8, head_dependent=True))
+
+
+@pytest.mark.parametrize("name", ["cfg1", "cfg2", "cfg3", "cfg4b"])
+def test_workload_tables(name):
+    w = {"cfg1": workloads.cfg1, "cfg2": workloads.cfg2, "cfg3": workloads.cfg3,
+         "cfg4b": lambda: workloads.cfg4(n=8192)}[name]()
+    bm, t = gpu_tables(w.rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk, doc=w.doc_ids)
+    want = orc.block_mask(w.rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk, doc_ids=w.doc_ids)
+    assert_tables_equal(t, want)
+    st = fa.block_mask_stats(bm).cpu().tolist()
+    cls = want["block_class"]
+    assert st[0] == int((cls == 2).sum()) and st[1] == int((cls == 1).sum()) and st[2] == int((cls == 0).sum())
+    if name == "cfg1":
+        assert (st[0], st[1]) == (7, 14)
+    if name == "cfg2":
+        assert (st[0], st[1], st[2]) == (496, 32, 496)
+    if name == "cfg4b":
+        assert (st[0], st[1]) == (420, 120)
+
+
+def test_cfg4_full_size_table():
+    w = workloads.cfg4()
+    bm, t = gpu_tables(w.rule, 1, w.Hq, w.q_len, w.kv_len, 128, 128)
+    st = fa.block_mask_stats(bm).cpu().tolist()
+    assert (st[0], st[1], st[3]) == (3556, 1016, 9)       # full, partial, longest row (window 1024 / 128 + 1)
+    rows = sorted({0, 1, 7, 8, 9, 100, 255, 256, 511} | set(np.random.default_rng(4).integers(0, 512, 24).tolist()))
+    want = orc.block_mask(w.rule, 1, w.Hq, w.q_len, w.kv_len, 128, 128, rows=rows)
+    assert_tables_equal(t, want, rows=rows)
+    # the transpose agrees with the forward table (checked on the whole table, on the device copy)
+    dense_f = np.zeros((512, 512), bool)
+    dense_t = np.zeros((512, 512), bool)
+    for r in range(512):
+        dense_f[r, t["kv_idx"][0, 0, r, :t["kv_num"][0, 0, r]]] = True
+    for c in range(512):
+        dense_t[t["q_idx"][0, 0, c, :t["q_num"][0, 0, c]], c] = True
+    assert np.array_equal(dense_f, dense_t)
+
+
+def test_cfg5_decode_table():
+    d = workloads.cfg5()
+    off = d.q_offset
+    _, t = gpu_tables(d.rule, d.Bz, d.Hq, 1, d.kv_len, 1, d.page, q_off=off, bdep=True)
+    want = orc.block_mask(d.rule, d.Bz, d.Hq, 1, d.kv_len, 1, d.page, batch_dependent=True, q_offset=off)
+    assert_tables_equal(t, want)
+    L = d.kv_lens
+    assert np.array_equal(t["full_kv_num"][:, 0, 0], L // 128)
+    assert np.array_equal(t["kv_num"][:, 0, 0], (L % 128 != 0).astype(np.int32))
+    dp = workloads.cfg5(prefix=512)
+    _, tp = gpu_tables(dp.rule, dp.Bz, dp.Hq, 1, dp.kv_len, 1, dp.page, q_off=off, bdep=True)
+    assert_tables_equal(tp, t)      # the prefix region is already visible at every cur_pos >= 1023
