@@ -201,7 +201,7 @@ def ours(args, rank, world, local_rank):
     sc = fa.make_score_rule(al, None, w.score.get("softcap", 0.0))
     rule = fa.make_mask_rule(w.rule, doc_ids=doc)
     bm = fa.create_block_mask(rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk, device=dev, keep=[doc])
-    out = torch.empty_like(q)
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)   # O stored in fp32 (accumulator precision)
     lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stats = fa.block_mask_stats(bm).cpu().tolist()
@@ -269,7 +269,7 @@ def ours(args, rank, world, local_rank):
         hq = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True).copy_(q)
         hk = torch.empty(k.shape, dtype=torch.bfloat16, pin_memory=True).copy_(k)
         hv = torch.empty(v.shape, dtype=torch.bfloat16, pin_memory=True).copy_(v)
-        ho = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
+        ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         hl = torch.empty(lse.shape, dtype=torch.float32, pin_memory=True)
 
         def e2e_step():
@@ -293,7 +293,7 @@ def ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         e2e_ms = s2.elapsed_time(e2) / n2
         bi = 3 * q.numel() * 2
-        bo = out.numel() * 2 + lse.numel() * 4
+        bo = out.numel() * out.element_size() + lse.numel() * 4
         e2e = {"value": world * phys_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
 
@@ -319,8 +319,8 @@ def ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} N={w.q_len} d={w.d} Bq=Bk={w.bq}",
-                   "step": "fa_create_block_mask + fa_flex_forward", "l2": "inputs 3x64 MiB + output > 129 MB L2 "
-                   "(no flush)", "parallelism": f"replica x{world} (independent (b,h) shards, no collective)"},
+                   "step": "fa_create_block_mask + fa_flex_forward", "out": "fp32 O, fp32 LSE",
+                   "l2": "inputs 3x64 MiB + 128 MiB output > 129 MB L2 (no flush)", "parallelism": f"replica x{world} (independent (b,h) shards, no collective)"},
         "physical_tflop_per_step": phys_flops / 1e12,
         "logical_tflops": (world * 4.0 * w.d * logical_pairs / (ms_step * 1e-3) / 1e12) if logical_pairs else None,
         "pct_bf16_peak": value / world / pk["bf16"],

@@ -231,10 +231,11 @@ __global__ void __launch_bounds__(kDecWarps * 32)
       for (int nt = 0; nt < 4; ++nt) {
         const float p0 = ex2_approx(sc[nt][0] - ref_a), p1 = ex2_approx(sc[nt][1] - ref_a);
         const float p2 = ex2_approx(sc[nt][2] - ref_b), p3 = ex2_approx(sc[nt][3] - ref_b);
-        ps_a += p0 + p1;
-        ps_b += p2 + p3;
-        pf[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-        pf[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+        const uint32_t pa = pack_bf16x2(p0, p1), pb = pack_bf16x2(p2, p3);
+        pf[nt >> 1][(nt & 1) * 2 + 0] = pa;
+        pf[nt >> 1][(nt & 1) * 2 + 1] = pb;
+        ps_a += bf16x2_sum(pa);  // row sums of the rounded P the product uses
+        ps_b += bf16x2_sum(pb);
       }
       l_a = l_a * al_a + ps_a;
       l_b = l_b * al_b + ps_b;
@@ -330,7 +331,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
   const int n_vis = __ldg(M.full_kv_num + mrow) + __ldg(M.kv_num + mrow);
   const int ns = (n_vis + a.pages_per_split - 1) / a.pages_per_split;
   const size_t base = ((size_t)b * a.Hq + hq) * (size_t)a.n_splits;
-  __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)b * a.Hq + hq) * D;
+  const size_t obase = ((size_t)b * a.Hq + hq) * D;
   float mm = -INFINITY;
   for (int s = 0; s < ns; ++s) mm = fmaxf(mm, a.ws_m[base + s]);
   const float ref = mm == -INFINITY ? 0.f : mm;
@@ -341,7 +342,10 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
   for (int col = threadIdx.x; col < D; col += blockDim.x) {
     float u = 0.f;
     for (int s = 0; s < ns; ++s) u += ex2_approx(a.ws_m[base + s] - ref) * a.ws_u[(base + s) * D + col];
-    O[col] = __float2bfloat16_rn(u * inv);
+    if (a.out_f32)
+      reinterpret_cast<float*>(a.out)[obase + col] = u * inv;
+    else
+      reinterpret_cast<__nv_bfloat16*>(a.out)[obase + col] = __float2bfloat16_rn(u * inv);
   }
   if (threadIdx.x == 0) a.lse[(size_t)b * a.Hq + hq] = empty ? -INFINITY : (mm + __log2f(l)) * kLn2;
 }

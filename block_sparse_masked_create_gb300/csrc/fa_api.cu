@@ -173,8 +173,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-int encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                     const uint64_t* strides_bytes, const uint32_t* box) {
+static int encode_tmap(CUtensorMapDataType dt, CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
   if (!enc) return -1;
   cuuint64_t gd[5], gs[4];
@@ -185,10 +185,20 @@ int encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t*
     es[i] = 1;
   }
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
+  CUresult r = enc(m, dt, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+int encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tmap(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m, base, rank, dims, strides_bytes, box);
+}
+
+int encode_tmap_f32(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tmap(CU_TENSOR_MAP_DATA_TYPE_FLOAT32, m, base, rank, dims, strides_bytes, box);
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -215,11 +225,13 @@ static int check_forward(const void* q, const void* k, const void* v, const fa_b
 }
 
 static int forward_impl(bool force_mma, const void* q, const void* k, const void* v, const fa_block_mask* bm,
-                        const fa_score_rule* score, float scale, void* out, float* lse, int32_t B, int32_t Hq,
+                        const fa_score_rule* score, float scale, void* out, int32_t out_dtype, float* lse,
+                        int32_t B, int32_t Hq,
                         int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d, int32_t* dev_status,
                         int64_t* dev_counters, fa_stream_t stream) {
   int s = check_forward(q, k, v, bm, out, lse, B, Hq, Hkv, Q_LEN, KV_LEN, d);
   if (s != FA_OK) return s;
+  if (out_dtype != FA_OUT_BF16 && out_dtype != FA_OUT_F32) return FA_ERR_INVALID_ARG;
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
   s = compile_rule(&bm->rule, &a.rule);
@@ -228,6 +240,7 @@ static int forward_impl(bool force_mma, const void* q, const void* k, const void
   a.k = k;
   a.v = v;
   a.out = out;
+  a.out_f32 = out_dtype == FA_OUT_F32;
   a.lse = lse;
   a.B = B;
   a.Hq = Hq;
@@ -341,19 +354,19 @@ fa_status fa_create_block_mask(const fa_mask_rule* rule, int32_t B, int32_t H, i
 }
 
 fa_status fa_flex_forward(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
-                          const fa_score_rule* score_rule, float scale, void* out, float* lse, int32_t B,
-                          int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d, int32_t* dev_status,
-                          int64_t* dev_counters, fa_stream_t stream) {
-  return (fa_status)forward_impl(false, q, k, v, block_mask, score_rule, scale, out, lse, B, Hq, Hkv, Q_LEN, KV_LEN,
-                                 d, dev_status, dev_counters, stream);
+                          const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype, float* lse,
+                          int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d,
+                          int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream) {
+  return (fa_status)forward_impl(false, q, k, v, block_mask, score_rule, scale, out, out_dtype, lse, B, Hq, Hkv, Q_LEN,
+                                 KV_LEN, d, dev_status, dev_counters, stream);
 }
 
 fa_status fa_flex_forward_mma(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
-                              const fa_score_rule* score_rule, float scale, void* out, float* lse, int32_t B,
-                              int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d,
-                              int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream) {
-  return (fa_status)forward_impl(true, q, k, v, block_mask, score_rule, scale, out, lse, B, Hq, Hkv, Q_LEN, KV_LEN,
-                                 d, dev_status, dev_counters, stream);
+                              const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype,
+                              float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN,
+                              int32_t d, int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream) {
+  return (fa_status)forward_impl(true, q, k, v, block_mask, score_rule, scale, out, out_dtype, lse, B, Hq, Hkv, Q_LEN,
+                                 KV_LEN, d, dev_status, dev_counters, stream);
 }
 
 size_t fa_decode_workspace_bytes(int32_t Bz, int32_t Hq, int32_t d, int32_t max_pages, int32_t page) {
@@ -366,13 +379,15 @@ size_t fa_decode_workspace_bytes(int32_t Bz, int32_t Hq, int32_t d, int32_t max_
 
 fa_status fa_flex_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
                          int32_t n_pages_total, const fa_block_mask* bm, const fa_score_rule* score_rule,
-                         float scale, void* out, float* lse, int32_t Bz, int32_t Hq, int32_t Hkv, int32_t d,
+                         float scale, void* out, int32_t out_dtype, float* lse, int32_t Bz, int32_t Hq, int32_t Hkv,
+                         int32_t d,
                          int32_t page, int32_t max_pages, void* workspace, size_t workspace_bytes,
                          int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream) {
   if (!q || !k_pages || !v_pages || !page_table || !bm || !out || !lse || !workspace) return FA_ERR_INVALID_ARG;
   if (Bz < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || n_pages_total < 1 || max_pages < 1) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (page != 32 && page != 64 && page != 128 && page != 256) return FA_ERR_UNSUPPORTED;
+  if (page != 32 && page != 64 && page != 128) return FA_ERR_UNSUPPORTED;
+  if (out_dtype != FA_OUT_BF16 && out_dtype != FA_OUT_F32) return FA_ERR_INVALID_ARG;
   if (Hq / Hkv > 16) return FA_ERR_UNSUPPORTED;
   if (bm->bq != 1 || bm->bk != page || bm->q_len != 1 || (int64_t)bm->kv_len != (int64_t)max_pages * page ||
       bm->Hm != 1 || !(bm->Bm == 1 || bm->Bm == Bz) || bm->nk != max_pages || bm->nq != 1)
@@ -392,6 +407,7 @@ fa_status fa_flex_decode(const void* q, const void* k_pages, const void* v_pages
   a.page_table = page_table;
   a.n_pages_total = n_pages_total;
   a.out = out;
+  a.out_f32 = out_dtype == FA_OUT_F32;
   a.lse = lse;
   a.Bz = Bz;
   a.Hq = Hq;

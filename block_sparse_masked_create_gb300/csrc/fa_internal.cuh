@@ -325,6 +325,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// sum of the two bf16 halves of a packed pair, in fp32 (exact widening)
+__device__ __forceinline__ float bf16x2_sum(uint32_t v) {
+  return __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
+}
+
 __device__ __forceinline__ void cp_async_16(uint32_t saddr, const void* gptr, bool pred) {
   int sz = pred ? 16 : 0;  // zero-fill when pred is false
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(gptr), "r"(sz) : "memory");

@@ -39,6 +39,7 @@ struct FwdArgs {
   const void* k;
   const void* v;
   void* out;
+  int32_t out_f32;  // 1: O stored as fp32, 0: bf16
   float* lse;
   int32_t B, Hq, Hkv, q_len, kv_len, d;
   float scale;
@@ -61,6 +62,7 @@ struct DecArgs {
   const int32_t* page_table;
   int32_t n_pages_total;
   void* out;
+  int32_t out_f32;
   float* lse;
   int32_t Bz, Hq, Hkv, d, page, max_pages;
   float scale;
@@ -80,8 +82,10 @@ int launch_decode(const DecArgs& a, cudaStream_t st);
 
 cudaError_t launch_debug_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t st);
 
-// Host helper: encode a bf16 tensor map (dims innermost first) with 128-byte swizzle.
+// Host helpers: encode a bf16 / fp32 tensor map (dims innermost first) with 128-byte swizzle.
 int encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                      const uint64_t* strides_bytes /* rank-1 entries */, const uint32_t* box);
+int encode_tmap_f32(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
 
 }  // namespace fa

@@ -70,10 +70,12 @@ __global__ void __launch_bounds__(MmaCfg<D, BQ, BK>::kThreads)
   const int row_b = row_a + 8;
 
   if (n_vis == 0) {  // empty row block: O = 0, LSE = -inf, no K/V loads
-    constexpr int kChunks = D / 8;
+    const int kChunks = a.out_f32 ? D / 4 : D / 8;  // 16-byte chunks per row
+    uint8_t* Ob = reinterpret_cast<uint8_t*>(a.out) + ((size_t)b * a.Hq + h) * a.q_len * D * (a.out_f32 ? 4 : 2);
     for (int x = tid; x < BQ * kChunks; x += C::kThreads) {
       int rr = x / kChunks, ch = x % kChunks;
-      if (q0 + rr < a.q_len) *reinterpret_cast<uint4*>(Og + (size_t)(q0 + rr) * D + ch * 8) = make_uint4(0, 0, 0, 0);
+      if (q0 + rr < a.q_len)
+        *reinterpret_cast<uint4*>(Ob + ((size_t)(q0 + rr) * kChunks + ch) * 16) = make_uint4(0, 0, 0, 0);
     }
     for (int x = tid; x < BQ; x += C::kThreads)
       if (q0 + x < a.q_len) Lg[q0 + x] = -INFINITY;
@@ -221,11 +223,13 @@ __global__ void __launch_bounds__(MmaCfg<D, BQ, BK>::kThreads)
     for (int nt = 0; nt < BK / 8; ++nt) {
       const float p0 = ex2_approx(s[nt][0] - ref_a), p1 = ex2_approx(s[nt][1] - ref_a);
       const float p2 = ex2_approx(s[nt][2] - ref_b), p3 = ex2_approx(s[nt][3] - ref_b);
-      ps_a += p0 + p1;
-      ps_b += p2 + p3;
-      // C-fragment of n-tiles (2k, 2k+1) -> A-fragment of k-step k
-      pf[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-      pf[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+      // C-fragment of n-tiles (2k, 2k+1) -> A-fragment of k-step k; the row sums use the rounded P that
+      // the P V product sees, so O is an exact convex combination of the V rows
+      const uint32_t pa = pack_bf16x2(p0, p1), pb = pack_bf16x2(p2, p3);
+      pf[nt >> 1][(nt & 1) * 2 + 0] = pa;
+      pf[nt >> 1][(nt & 1) * 2 + 1] = pb;
+      ps_a += bf16x2_sum(pa);
+      ps_b += bf16x2_sum(pb);
     }
     l_a = l_a * al_a + ps_a;
     l_b = l_b * al_b + ps_b;
@@ -258,6 +262,20 @@ __global__ void __launch_bounds__(MmaCfg<D, BQ, BK>::kThreads)
   l_b += __shfl_xor_sync(0xFFFFFFFFu, l_b, 2);
   const bool emp_a = m_a == -INFINITY, emp_b = m_b == -INFINITY;
   const float inv_a = emp_a ? 0.f : 1.f / l_a, inv_b = emp_b ? 0.f : 1.f / l_b;
+  if ((lane & 3) == 0) {
+    if (row_a < a.q_len) Lg[row_a] = emp_a ? -INFINITY : (m_a + __log2f(l_a)) * kLn2;
+    if (row_b < a.q_len) Lg[row_b] = emp_b ? -INFINITY : (m_b + __log2f(l_b)) * kLn2;
+  }
+  if (a.out_f32) {
+    float* Of = reinterpret_cast<float*>(a.out) + ((size_t)b * a.Hq + h) * a.q_len * D;
+#pragma unroll
+    for (int dt = 0; dt < D / 8; ++dt) {
+      const int col = dt * 8 + (lane & 3) * 2;
+      if (row_a < a.q_len) *reinterpret_cast<float2*>(Of + (size_t)row_a * D + col) = make_float2(o[dt][0] * inv_a, o[dt][1] * inv_a);
+      if (row_b < a.q_len) *reinterpret_cast<float2*>(Of + (size_t)row_b * D + col) = make_float2(o[dt][2] * inv_b, o[dt][3] * inv_b);
+    }
+    return;
+  }
   // stage O through this warp's own Q rows in shared memory, then 16-byte coalesced stores
 #pragma unroll
   for (int dt = 0; dt < D / 8; ++dt) {
@@ -265,10 +283,6 @@ __global__ void __launch_bounds__(MmaCfg<D, BQ, BK>::kThreads)
     const int ra = warp * 16 + (lane >> 2), rb = ra + 8;
     *reinterpret_cast<uint32_t*>(sQ + swz<D>(ra, col >> 3) + (col & 7) * 2) = pack_bf16x2(o[dt][0] * inv_a, o[dt][1] * inv_a);
     *reinterpret_cast<uint32_t*>(sQ + swz<D>(rb, col >> 3) + (col & 7) * 2) = pack_bf16x2(o[dt][2] * inv_b, o[dt][3] * inv_b);
-  }
-  if ((lane & 3) == 0) {
-    if (row_a < a.q_len) Lg[row_a] = emp_a ? -INFINITY : (m_a + __log2f(l_a)) * kLn2;
-    if (row_b < a.q_len) Lg[row_b] = emp_b ? -INFINITY : (m_b + __log2f(l_b)) * kLn2;
   }
   __syncwarp();
   for (int x = lane; x < 16 * kChunks; x += 32) {

@@ -1,5 +1,574 @@
-// placeholder: replaced by the tcgen05 forward kernel
+// Block-sparse masked attention forward on 5th-generation tensor cores (tcgen05, accumulators in tensor
+// memory), 128 x 128 blocks, head dim 64 or 128.
+//
+// What it computes is "5.1.2 FlexAttention: from rules to fused kernels", section 3.1 (and
+// "FlexAttention: compiler optimisation of custom attention", section 3): per query block, visit the
+// BlockMask's full blocks without the mask and its partial blocks with it; per block S = scale * Q K^T,
+// score rule, -inf for masked pairs (partial blocks only), online softmax (m, l), acc += P V; finally
+// O = acc / l and LSE = m + ln l, an empty row giving O = 0, LSE = -inf.
+//
+// How (one CTA = two 128-row query tiles of sibling heads of the same query block, 10 warps):
+//   warps 0-3 / 4-7  softmax warpgroups of tile 0 / tile 1: S from TMEM to registers (one row per
+//                    thread), score rule, mask, row max, exp2, row sum; P as bf16 into shared memory in
+//                    the 128-byte-swizzled K-major layout the MMA reads; rescale of the O accumulator in
+//                    TMEM only when the running max grows by more than 2^8 (the result is exact for any
+//                    reference max; the bound keeps P <= 256); epilogue O / l -> bf16 -> TMA store.
+//   warp 8           TMA producer: Q tiles, then K / V tiles of the visited blocks only (an empty block
+//                    issues no load) into a ring of shared-memory slots, in exactly the order the MMA
+//                    warp consumes them. Sibling query heads of one KV head with the same mask row share
+//                    each K / V load.
+//   warp 9           allocates TMEM (512 columns: S and O of both tiles) and issues every tcgen05.mma from
+//                    one thread: S_t = Q_t K^T (A, B K-major), O_t += P_t V (A K-major, B = V MN-major);
+//                    completion is signalled with tcgen05.commit on mbarriers.
+// The two tiles ping-pong: while one warpgroup works on its softmax, the tensor core runs the other
+// tile's MMAs. Every wait is bounded (an abort flag stops all roles; copies and MMAs in flight are
+// drained before tensor memory is freed and the CTA exits).
+#include <cstring>
+
 #include "fa_launch.h"
+
 namespace fa {
-int launch_fwd_tc5(const FwdArgs&, cudaStream_t) { return FA_ERR_UNSUPPORTED; }
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 2^8
+
+enum ScoreKind { SK_NONE = 0, SK_ALIBI = 1, SK_SOFTCAP = 2, SK_GENERIC = 3 };
+
+template <int D>
+struct Tc5Cfg {
+  static constexpr int kQBytes = 128 * D * 2;      // one Q tile
+  static constexpr int kPBytes = 128 * 128 * 2;    // one P tile (also the O staging tile)
+  static constexpr int kSlotBytes = 128 * D * 2;   // one K or V tile
+  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int kOffP = 2 * kQBytes;
+  static constexpr int kOffRing = kOffP + 2 * kPBytes;
+  static constexpr int kSmem = kOffRing + kStages * kSlotBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  // tensor-memory columns: S of tile t at [256 t, 256 t + 128), O of tile t at [256 t + 128, 256 t + 128 + D)
+  __device__ static constexpr uint32_t col_s(int t) { return (uint32_t)t * 256u; }
+  __device__ static constexpr uint32_t col_o(int t) { return (uint32_t)t * 256u + 128u; }
+};
+
+struct Tc5Params {
+  FwdArgs a;
+  int n_pairs, heads_per_pair_groups;  // pairs = B * nq * ceil(Hq / 2)
+};
+
+// byte offset of 16-byte chunk c16 of row `row` in a [128][D] tile stored as D/64 sub-tiles [128][64]
+// with the 128-byte swizzle (TMA SWIZZLE_128B layout; also the UMMA K-major SW128 layout)
+__device__ __forceinline__ uint32_t tile_off(int row, int c16) {
+  return (uint32_t)((c16 >> 3) * 16384 + row * 128 + (((c16 & 7) ^ (row & 7)) << 4));
 }
+
+struct Tile {
+  int valid;     // a tile exists (Hq may be odd)
+  int h, hk;     // query head, KV head
+  int n_full, n_part, n;
+  const int32_t* full_idx;
+  const int32_t* part_idx;
+  __device__ __forceinline__ int col(int j) const { return j < n_full ? __ldg(full_idx + j) : __ldg(part_idx + j - n_full); }
+};
+
+template <int D, int SK>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc5_kernel(const __grid_constant__ Tc5Params P, const __grid_constant__ CUtensorMap tmQ,
+                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmO) {
+  using C = Tc5Cfg<D>;
+  constexpr int NST = C::kStages;
+  const FwdArgs& a = P.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_q[2], bar_s[2], bar_p[2], bar_o[2], bar_full[NST], bar_empty[NST], bar_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int32_t s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- work item: (query block r, batch b, head pair hp); heaviest query blocks first for causal
+  const int HP = (a.Hq + 1) / 2;
+  const DevMask& M = a.mask;
+  int p = blockIdx.x;
+  const int hp = p % HP;
+  p /= HP;
+  const int b = p % a.B;
+  const int r = M.nq - 1 - p / a.B;
+  const int g = a.Hq / a.Hkv;
+  Tile T[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int h = 2 * hp + t;
+    T[t].valid = h < a.Hq;
+    T[t].h = T[t].valid ? h : 0;
+    T[t].hk = T[t].h / g;
+    const int bm = M.Bm > 1 ? b : 0, hm = M.Hm > 1 ? T[t].h : 0;
+    const size_t mrow = ((size_t)bm * M.Hm + hm) * M.nq + r;
+    T[t].n_full = T[t].valid ? __ldg(M.full_kv_num + mrow) : 0;
+    T[t].n_part = T[t].valid ? __ldg(M.kv_num + mrow) : 0;
+    T[t].n = T[t].n_full + T[t].n_part;
+    T[t].full_idx = M.full_kv_idx + mrow * M.nk;
+    T[t].part_idx = M.kv_idx + mrow * M.nk;
+  }
+  // sibling heads of one KV head with the same mask row share K / V loads
+  const bool shared_kv = T[1].valid && T[0].hk == T[1].hk && T[0].n > 0 && M.Hm == 1;
+  const int nmax = max(T[0].n, T[1].n);
+
+  uint8_t* sQ[2] = {smem, smem + C::kQBytes};
+  uint8_t* sP[2] = {smem + C::kOffP, smem + C::kOffP + C::kPBytes};
+  uint8_t* sRing = smem + C::kOffRing;
+
+  if (tid == 0) {
+    s_abort = 0;
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar_q[t], 1);
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_p[t], 128);
+      mbar_init(&bar_o[t], 1);
+    }
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(&bar_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&s_tmem, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
+  }
+  tc5_fence_before();
+  __syncthreads();
+  tc5_fence_after();
+  const uint32_t tmem = s_tmem;
+  WaitCtl wc{a.timeout_ns, a.status, &s_abort};
+
+  if (warp == kLoadWarp) {
+    // =============================== TMA producer ===============================
+    if (lane == 0) {
+      if (a.counters) {
+        unsigned long long* cnt = reinterpret_cast<unsigned long long*>(a.counters);
+        const int vis = T[0].n + T[1].n;
+        atomicAdd(cnt + 0, (unsigned long long)(T[0].valid + T[1].valid));
+        atomicAdd(cnt + 1, (unsigned long long)(T[0].n_full + T[1].n_full));
+        atomicAdd(cnt + 2, (unsigned long long)(T[0].n_part + T[1].n_part));
+        atomicAdd(cnt + 3, (unsigned long long)(shared_kv ? vis : 2 * vis));
+      }
+      for (int t = 0; t < 2; ++t) {
+        if (T[t].n == 0) continue;
+        mbar_arrive_expect_tx(&bar_q[t], C::kQBytes);
+#pragma unroll
+        for (int x = 0; x < D / 64; ++x)
+          tma_load_3d(sQ[t] + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T[t].h, &bar_q[t]);
+      }
+      int issued = 0;
+      bool ok = true;
+      auto load = [&](int t, bool is_v, int j) -> bool {
+        const int s = issued % NST;
+        if (issued >= NST && !mbar_wait(&bar_empty[s], (uint32_t)(((issued / NST) - 1) & 1), wc)) return false;
+        const int c = T[t].col(j);
+        uint8_t* dst = sRing + s * C::kSlotBytes;
+        mbar_arrive_expect_tx(&bar_full[s], C::kSlotBytes);
+#pragma unroll
+        for (int x = 0; x < D / 64; ++x)
+          tma_load_3d(dst + x * 16384, is_v ? &tmV : &tmK, x * 64, c * 128, b * a.Hkv + T[t].hk, &bar_full[s]);
+        ++issued;
+        return true;
+      };
+      if (shared_kv) {
+        ok = load(0, false, 0);
+        for (int j = 1; j <= T[0].n && ok; ++j) {
+          ok = load(0, true, j - 1);
+          if (ok && j < T[0].n) ok = load(0, false, j);
+        }
+      } else {
+        for (int t = 0; t < 2 && ok; ++t)
+          if (T[t].n > 0) ok = load(t, false, 0);
+        for (int j = 1; j <= nmax && ok; ++j)
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j - 1 < T[t].n) ok = load(t, true, j - 1);
+            if (ok && j < T[t].n) ok = load(t, false, j);
+          }
+      }
+      if (!ok || *wc.abort) {
+        // drain: the last NST issued copies may still be landing in shared memory
+        for (int i = max(0, issued - NST); i < issued; ++i)
+          mbar_wait_drain(&bar_full[i % NST], (uint32_t)((i / NST) & 1), a.timeout_ns);
+        for (int t = 0; t < 2; ++t)
+          if (T[t].n > 0) mbar_wait_drain(&bar_q[t], 0, a.timeout_ns);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // =============================== MMA issuer ===============================
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+      int consumed = 0;
+      bool ok = true;
+      for (int t = 0; t < 2 && ok; ++t)
+        if (T[t].n > 0) ok = mbar_wait(&bar_q[t], 0, wc);
+      tc5_fence_after();
+      auto take = [&]() -> int {  // wait for the next ring slot in load order
+        const int s = consumed % NST;
+        if (!mbar_wait(&bar_full[s], (uint32_t)((consumed / NST) & 1), wc)) return -1;
+        tc5_fence_after();
+        ++consumed;
+        return s;
+      };
+      auto mma_qk = [&](int t, int s) {
+        const uint32_t qa = smem_u32(sQ[t]), ka = smem_u32(sRing + s * C::kSlotBytes);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          tc5_mma_ss(tmem + C::col_s(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_qk,
+                     ks > 0 ? 1u : 0u);
+        }
+      };
+      auto mma_pv = [&](int t, int s, bool acc) {
+        const uint32_t pa = smem_u32(sP[t]), va = smem_u32(sRing + s * C::kSlotBytes);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t offp = (ks >> 2) * 16384 + (ks & 3) * 32;
+          tc5_mma_ss(tmem + C::col_o(t), sdesc_sw128(pa + offp, 16, 1024),
+                     sdesc_sw128(va + ks * 2048, 128 * 128, 1024), idesc_pv, (acc || ks > 0) ? 1u : 0u);
+        }
+      };
+      if (ok) {
+        if (shared_kv) {
+          const int n = T[0].n;
+          int sk = take();
+          ok = sk >= 0;
+          if (ok) {
+            mma_qk(0, sk);
+            tc5_commit(&bar_s[0]);
+            mma_qk(1, sk);
+            tc5_commit(&bar_s[1]);
+            tc5_commit(&bar_empty[sk]);
+          }
+          for (int j = 1; j <= n && ok; ++j) {
+            ok = mbar_wait(&bar_p[0], (uint32_t)((j - 1) & 1), wc);
+            if (!ok) break;
+            tc5_fence_after();
+            const int sv = take();
+            if (sv < 0) { ok = false; break; }
+            mma_pv(0, sv, j > 1);
+            tc5_commit(&bar_o[0]);
+            int sk2 = -1;
+            if (j < n) {
+              sk2 = take();
+              if (sk2 < 0) { ok = false; break; }
+              mma_qk(0, sk2);
+              tc5_commit(&bar_s[0]);
+            }
+            ok = mbar_wait(&bar_p[1], (uint32_t)((j - 1) & 1), wc);
+            if (!ok) break;
+            tc5_fence_after();
+            mma_pv(1, sv, j > 1);
+            tc5_commit(&bar_o[1]);
+            tc5_commit(&bar_empty[sv]);
+            if (j < n) {
+              mma_qk(1, sk2);
+              tc5_commit(&bar_s[1]);
+              tc5_commit(&bar_empty[sk2]);
+            }
+          }
+        } else {
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (T[t].n == 0) continue;
+            const int s = take();
+            if (s < 0) { ok = false; break; }
+            mma_qk(t, s);
+            tc5_commit(&bar_s[t]);
+            tc5_commit(&bar_empty[s]);
+          }
+          for (int j = 1; j <= nmax && ok; ++j) {
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (j - 1 >= T[t].n) continue;
+              ok = mbar_wait(&bar_p[t], (uint32_t)((j - 1) & 1), wc);
+              if (!ok) break;
+              tc5_fence_after();
+              const int sv = take();
+              if (sv < 0) { ok = false; break; }
+              mma_pv(t, sv, j > 1);
+              tc5_commit(&bar_o[t]);
+              tc5_commit(&bar_empty[sv]);
+              if (j < T[t].n) {
+                const int sk = take();
+                if (sk < 0) { ok = false; break; }
+                mma_qk(t, sk);
+                tc5_commit(&bar_s[t]);
+                tc5_commit(&bar_empty[sk]);
+              }
+            }
+          }
+        }
+      }
+      // every MMA issued so far has completed before tensor memory is read back or freed
+      tc5_commit(&bar_drain);
+      mbar_wait_drain(&bar_drain, 0, a.timeout_ns);
+    }
+  } else {
+    // =============================== softmax warpgroups ===============================
+    const int t = warp >> 2;                 // tile of this warpgroup
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane == query row in the tile
+    const Tile& TT = T[t];
+    const int q_row = r * 128 + row;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + C::col_s(t);
+    const uint32_t tO = tmem + lane_base + C::col_o(t);
+    float* Lg = a.lse + ((size_t)b * a.Hq + TT.h) * a.q_len;
+    if (TT.valid && TT.n == 0) {
+      // empty query block: O = 0, LSE = -inf, nothing loaded
+      __nv_bfloat16* Og = reinterpret_cast<__nv_bfloat16*>(a.out) + (((size_t)b * a.Hq + TT.h) * a.q_len) * D;
+      if (q_row < a.q_len) {
+        uint4 z = make_uint4(0, 0, 0, 0);
+        for (int c16 = 0; c16 < D / 8; ++c16) *reinterpret_cast<uint4*>(Og + (size_t)q_row * D + c16 * 8) = z;
+        Lg[q_row] = -INFINITY;
+      }
+    } else if (TT.valid) {
+      const int64_t off_b = a.rule.q_offset ? (int64_t)__ldg(a.rule.q_offset + (M.Bm > 1 ? b : 0)) : 0;
+      const int64_t ig = (int64_t)q_row + off_b;
+      const int bm = M.Bm > 1 ? b : 0;
+      const int doc_i = a.rule.any_doc ? doc_at(a.rule, bm, ig) : -1;
+      const float sl2 = a.scale * kLog2e;
+      float slope2 = 0.f;
+      if (SK == SK_ALIBI || SK == SK_GENERIC) slope2 = a.score.alibi ? __ldg(a.score.alibi + TT.h) * kLog2e : 0.f;
+      float m_ref = -INFINITY;  // reference max (log2 domain) used for P and for O
+      float l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < TT.n && ok; ++j) {
+        ok = mbar_wait(&bar_s[t], (uint32_t)(j & 1), wc);
+        if (!ok) break;
+        tc5_fence_after();
+        float x[128];
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) tc5_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&x[c0]));
+        tc5_wait_ld();
+        const bool partial = j >= TT.n_full;
+        const int c = TT.col(j);
+        const int64_t j0 = (int64_t)c * 128;
+        // ---- scale + score rule, in the log2 domain
+        if (SK == SK_NONE) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) x[i] *= sl2;
+        } else if (SK == SK_ALIBI) {
+          const float base = -slope2 * (float)(ig - j0);  // bias at column 0 (log2 units)
+#pragma unroll
+          for (int i = 0; i < 128; ++i) x[i] = fmaf(x[i], sl2, fmaf(slope2, (float)i, base));
+        } else if (SK == SK_SOFTCAP) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            x[i] = softcap_apply(x[i] * a.scale, a.score.softcap, a.score.inv_softcap) * kLog2e;
+        } else {
+          for (int i = 0; i < 128; ++i) {
+            float v = x[i] * a.scale;
+            const int64_t dist = ig - (j0 + i);
+            if (a.score.alibi) v -= (slope2 * kLn2) * (float)dist;
+            if (a.score.rel) {
+              int64_t ix = dist + a.score.kv_len - 1;
+              ix = ix < 0 ? 0 : (ix > 2 * (int64_t)a.score.kv_len - 2 ? 2 * (int64_t)a.score.kv_len - 2 : ix);
+              v += __ldg(a.score.rel + (size_t)TT.h * (2 * (size_t)a.score.kv_len - 1) + ix);
+            }
+            if (a.score.softcap > 0.f) v = softcap_apply(v, a.score.softcap, a.score.inv_softcap);
+            x[i] = v * kLog2e;
+          }
+        }
+        // ---- mask after the score rule, partial blocks only
+        if (partial) {
+          const int w = (int)min((int64_t)128, (int64_t)a.kv_len - j0);
+          Bits128 bits = {{0u, 0u, 0u, 0u}};
+          if (q_row < a.q_len) {
+            bits = rule_row_bits(a.rule, ig, j0, w, doc_i, [&](int dq) {
+              Bits128 db = {{0u, 0u, 0u, 0u}};
+              for (int cc = 0; cc < w; ++cc)
+                if (doc_at(a.rule, bm, j0 + cc) == dq) db.w[cc >> 5] |= 1u << (cc & 31);
+              return db;
+            });
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t wd = bits.w[k];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[k * 32 + i] = ((wd >> i) & 1u) ? x[k * 32 + i] : -INFINITY;
+          }
+        }
+        float mb = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) mb = fmaxf(mb, x[i]);
+        // ---- reference max: move it only when the block max exceeds it by more than 2^8
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mb > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mb > -INFINITY)) {
+          alpha = m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - mb);
+          rescale = j > 0 && m_ref != -INFINITY;
+          m_ref = mb;
+        }
+        const float mr = m_ref == -INFINITY ? 0.f : m_ref;
+        float rs = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float p0 = ex2_approx(x[2 * i] - mr), p1 = ex2_approx(x[2 * i + 1] - mr);
+          pk[i] = pack_bf16x2(p0, p1);
+          rs += bf16x2_sum(pk[i]);  // row sum of the rounded P the product uses
+        }
+        l = l * alpha + rs;
+        // ---- the previous P V must be complete: P buffer free, O stable
+        if (j > 0) {
+          ok = mbar_wait(&bar_o[t], (uint32_t)((j - 1) & 1), wc);
+          if (!ok) break;
+          tc5_fence_after();
+        }
+        if (rescale) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tc5_ld32(tO + c0, o);
+            tc5_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tc5_st32(tO + c0, o);
+          }
+          tc5_wait_st();
+        }
+        uint8_t* pbuf = sP[t];
+#pragma unroll
+        for (int c16 = 0; c16 < 16; ++c16)
+          *reinterpret_cast<uint4*>(pbuf + tile_off(row, c16)) =
+              make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+        fence_proxy_async_smem();
+        tc5_fence_before();
+        mbar_arrive(&bar_p[t]);
+      }
+      // ---- epilogue
+      if (ok) ok = mbar_wait(&bar_o[t], (uint32_t)((TT.n - 1) & 1), wc);
+      tc5_fence_after();
+      if (ok) {
+        const bool empty = m_ref == -INFINITY;
+        const float inv = empty ? 0.f : 1.f / l;
+        // staging for the TMA store (both buffers are free: the last Q K^T and P V have completed)
+        uint8_t* st = sP[t];
+        if (!a.out_f32) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tc5_ld32(tO + c0, o);
+            tc5_wait_ld();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
+              *reinterpret_cast<uint4*>(st + tile_off(row, c0 / 8 + q4)) = v;
+            }
+          }
+        } else {
+          // fp32: D/32 boxes of [128][32] floats (128-byte rows); boxes 0-1 in the P buffer, 2-3 in Q's
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tc5_ld32(tO + c0, o);
+            tc5_wait_ld();
+            uint8_t* box = (c0 < 64 ? sP[t] : sQ[t]) + ((c0 >> 5) & 1) * 16384;
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              float4 v = make_float4(__uint_as_float(o[4 * q4 + 0]) * inv, __uint_as_float(o[4 * q4 + 1]) * inv,
+                                     __uint_as_float(o[4 * q4 + 2]) * inv, __uint_as_float(o[4 * q4 + 3]) * inv);
+              *reinterpret_cast<float4*>(box + row * 128 + ((q4 ^ (row & 7)) << 4)) = v;
+            }
+          }
+        }
+        if (q_row < a.q_len) Lg[q_row] = empty ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
+      }
+      // every thread of the warpgroup reaches this barrier (ok or not); the store runs only if no role
+      // gave up (a failed wait always sets the CTA's abort flag)
+      fence_proxy_async_smem();
+      named_bar_sync(1 + t, 128);
+      if (!*wc.abort) {
+        uint8_t* st = sP[t];
+        if ((warp & 3) == 0 && lane == 0) {
+          if (!a.out_f32) {
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x) tma_store_3d(&tmO, st + x * 16384, x * 64, r * 128, b * a.Hq + TT.h);
+          } else {
+#pragma unroll
+            for (int x = 0; x < D / 32; ++x)
+              tma_store_3d(&tmO, (x < 2 ? sP[t] : sQ[t]) + (x & 1) * 16384, x * 32, r * 128, b * a.Hq + TT.h);
+          }
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+      }
+    }
+  }
+  tc5_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc5_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, int SK>
+int launch_k(const FwdArgs& a, cudaStream_t st) {
+  using C = Tc5Cfg<D>;
+  CUtensorMap tq, tk, tv, to;
+  const uint64_t dq[3] = {(uint64_t)D, (uint64_t)a.q_len, (uint64_t)a.B * a.Hq};
+  const uint64_t dk[3] = {(uint64_t)D, (uint64_t)a.kv_len, (uint64_t)a.B * a.Hkv};
+  const uint64_t sq[2] = {(uint64_t)D * 2, (uint64_t)a.q_len * D * 2};
+  const uint64_t sk[2] = {(uint64_t)D * 2, (uint64_t)a.kv_len * D * 2};
+  const uint32_t box[3] = {64, 128, 1};
+  if (encode_tmap_bf16(&tq, a.q, 3, dq, sq, box) || encode_tmap_bf16(&tk, a.k, 3, dk, sk, box) ||
+      encode_tmap_bf16(&tv, a.v, 3, dk, sk, box))
+    return FA_ERR_CUDA;
+  if (a.out_f32) {
+    const uint64_t so[2] = {(uint64_t)D * 4, (uint64_t)a.q_len * D * 4};
+    const uint32_t boxo[3] = {32, 128, 1};
+    if (encode_tmap_f32(&to, a.out, 3, dq, so, boxo)) return FA_ERR_CUDA;
+  } else if (encode_tmap_bf16(&to, a.out, 3, dq, sq, box)) {
+    return FA_ERR_CUDA;
+  }
+  Tc5Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.a = a;
+  const int HP = (a.Hq + 1) / 2;
+  p.n_pairs = a.B * a.mask.nq * HP;
+  auto kern = fwd_tc5_kernel<D, SK>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
+    return FA_ERR_CUDA;
+  kern<<<p.n_pairs, kThreads, C::kSmem, st>>>(p, tq, tk, tv, to);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int D>
+int launch_d(const FwdArgs& a, cudaStream_t st) {
+  const bool al = a.score.alibi != nullptr, rel = a.score.rel != nullptr, cap = a.score.softcap > 0.f;
+  if (!al && !rel && !cap) return launch_k<D, SK_NONE>(a, st);
+  if (al && !rel && !cap) return launch_k<D, SK_ALIBI>(a, st);
+  if (!al && !rel && cap) return launch_k<D, SK_SOFTCAP>(a, st);
+  return launch_k<D, SK_GENERIC>(a, st);
+}
+
+}  // namespace
+
+int launch_fwd_tc5(const FwdArgs& a, cudaStream_t st) {
+  if (a.mask.bq != 128 || a.mask.bk != 128) return FA_ERR_UNSUPPORTED;
+  if (a.B * (int64_t)a.mask.nq * ((a.Hq + 1) / 2) > 0x7FFFFFFF) return FA_ERR_UNSUPPORTED;
+  if (a.d == 128) return launch_d<128>(a, st);
+  if (a.d == 64) return launch_d<64>(a, st);
+  return FA_ERR_UNSUPPORTED;
+}
+
+}  // namespace fa

@@ -76,7 +76,7 @@ def load() -> ctypes.CDLL:
     lib.fa_block_mask_bytes.argtypes = [P(MaskRule), i32, i32, i32, i32, i32, i32]
     lib.fa_create_block_mask.restype = ctypes.c_int
     lib.fa_create_block_mask.argtypes = [P(MaskRule), i32, i32, i32, i32, i32, i32, vp, sz, P(BlockMaskC), vp]
-    fwd_args = [vp, vp, vp, P(BlockMaskC), P(ScoreRule), f32, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    fwd_args = [vp, vp, vp, P(BlockMaskC), P(ScoreRule), f32, vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.fa_flex_forward.restype = ctypes.c_int
     lib.fa_flex_forward.argtypes = fwd_args
     lib.fa_flex_forward_mma.restype = ctypes.c_int
@@ -84,7 +84,7 @@ def load() -> ctypes.CDLL:
     lib.fa_decode_workspace_bytes.restype = sz
     lib.fa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.fa_flex_decode.restype = ctypes.c_int
-    lib.fa_flex_decode.argtypes = [vp, vp, vp, vp, i32, P(BlockMaskC), P(ScoreRule), f32, vp, vp, i32, i32, i32, i32,
+    lib.fa_flex_decode.argtypes = [vp, vp, vp, vp, i32, P(BlockMaskC), P(ScoreRule), f32, vp, i32, vp, i32, i32, i32, i32,
                                    i32, i32, vp, sz, vp, vp, vp]
     lib.fa_block_mask_stats.restype = ctypes.c_int
     lib.fa_block_mask_stats.argtypes = [P(BlockMaskC), vp, vp]
@@ -236,26 +236,34 @@ def block_mask_stats(bm: BlockMask, out: Optional[torch.Tensor] = None) -> torch
 # ----------------------------------------------------------------------------------------------
 # attention
 # ----------------------------------------------------------------------------------------------
+def _out_code(out: torch.Tensor) -> int:
+    if out.dtype == torch.bfloat16:
+        return 0
+    if out.dtype == torch.float32:
+        return 1
+    raise ValueError("out must be bf16 or fp32")
+
+
 def flex_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: BlockMask,
                  score: Optional[ScoreRule] = None, scale: Optional[float] = None,
                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                  status: Optional[torch.Tensor] = None, counters: Optional[torch.Tensor] = None,
-                 force_mma: bool = False):
+                 force_mma: bool = False, out_dtype=torch.bfloat16):
     """fa_flex_forward: q [B,Hq,Q_LEN,d], k/v [B,Hkv,KV_LEN,d] bf16 contiguous on the GPU.
-    Returns (out bf16 [B,Hq,Q_LEN,d], lse fp32 [B,Hq,Q_LEN])."""
+    Returns (out [B,Hq,Q_LEN,d] in bf16 or fp32 (the dtype of `out`, else out_dtype), lse fp32 [B,Hq,Q_LEN])."""
     for t in (q, k, v):
         if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
             raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
     B, Hq, Q_LEN, d = q.shape
     Hkv, KV_LEN = k.shape[1], k.shape[2]
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Q_LEN), dtype=torch.float32, device=q.device)
     fn = load().fa_flex_forward_mma if force_mma else load().fa_flex_forward
     _check(fn(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(block_mask.c), ctypes.byref(score) if score else None,
-              float(scale) if scale else 0.0, _ptr(out), _ptr(lse), B, Hq, Hkv, Q_LEN, KV_LEN, d, _ptr(status),
-              _ptr(counters), _stream(q.device)), "fa_flex_forward")
+              float(scale) if scale else 0.0, _ptr(out), _out_code(out), _ptr(lse), B, Hq, Hkv, Q_LEN, KV_LEN, d,
+              _ptr(status), _ptr(counters), _stream(q.device)), "fa_flex_forward")
     return out, lse
 
 
@@ -267,13 +275,13 @@ def flex_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, p
                 block_mask: BlockMask, score: Optional[ScoreRule] = None, scale: Optional[float] = None,
                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                 workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                counters: Optional[torch.Tensor] = None):
+                counters: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16):
     """fa_flex_decode: q [Bz,Hq,d], k/v pages [P,Hkv,page,d] bf16, page_table int32 [Bz,max_pages]."""
     Bz, Hq, d = q.shape
     P, Hkv, page, _ = k_pages.shape
     max_pages = page_table.shape[1]
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((Bz, Hq), dtype=torch.float32, device=q.device)
     need = decode_workspace_bytes(Bz, Hq, d, max_pages, page)
@@ -281,9 +289,9 @@ def flex_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, p
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     _check(load().fa_flex_decode(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), P,
                                  ctypes.byref(block_mask.c), ctypes.byref(score) if score else None,
-                                 float(scale) if scale else 0.0, _ptr(out), _ptr(lse), Bz, Hq, Hkv, d, page, max_pages,
-                                 _ptr(workspace), workspace.numel(), _ptr(status), _ptr(counters),
-                                 _stream(q.device)), "fa_flex_decode")
+                                 float(scale) if scale else 0.0, _ptr(out), _out_code(out), _ptr(lse), Bz, Hq, Hkv,
+                                 d, page, max_pages, _ptr(workspace), workspace.numel(), _ptr(status),
+                                 _ptr(counters), _stream(q.device)), "fa_flex_decode")
     return out, lse
 
 

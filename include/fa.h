@@ -146,6 +146,10 @@ FA_API fa_status fa_create_block_mask(const fa_mask_rule* rule, int32_t B, int32
                                int32_t Bq, int32_t Bk, void* dev_buf, size_t buf_bytes, fa_block_mask* out,
                                fa_stream_t stream);
 
+/* Element type of O. The softmax statistics and the accumulator are fp32 in every case; FA_OUT_F32
+ * stores the fp32 result as is, FA_OUT_BF16 rounds it to bf16 (round to nearest even) on the store. */
+typedef enum { FA_OUT_BF16 = 0, FA_OUT_F32 = 1 } fa_out_dtype;
+
 /* flex_attention(q, k, v, score_mod, block_mask, scale) forward ("5.1.2 FlexAttention ...", section
  * 3.1: for each query block visit the full list without the mask and the partial list with it, keep the
  * online-softmax state (m, l, acc), write O = acc / l and LSE = m + ln l; an empty row writes O = 0,
@@ -156,24 +160,25 @@ FA_API fa_status fa_create_block_mask(const fa_mask_rule* rule, int32_t B, int32
  *                KV_LEN, Bm in {1, B}, Hm in {1, Hq} (a length mismatch is an error, never trimmed)
  *   score_rule   host pointer or NULL (no score rule)
  *   scale        > 0, or <= 0 for 1/sqrt(d)
- *   out          device bf16 [B, Hq, Q_LEN, d];   lse  device fp32 [B, Hq, Q_LEN] (natural log)
+ *   out          device [B, Hq, Q_LEN, d] of type out_dtype;  lse  device fp32 [B, Hq, Q_LEN] (natural log)
  *   dev_status   device int32 or NULL (device-side errors are then not reported)
  *   dev_counters device int64[4] or NULL: += {query tiles, full blocks visited, partial blocks visited,
- *                K/V tile loads issued} (for checking that empty blocks issue no loads)
+ *                K/V tile loads issued}. Empty blocks issue no load; a K/V tile load serves every query
+ *                tile of the CTA that reads it (sibling query heads of one KV head with one mask row).
  * Supported: d in {64, 128}; Bq, Bk in {16, 32, 64, 128}; Q_LEN, KV_LEN >= 1; Hq % Hkv == 0;
  * q/k/v/out 16-byte aligned. Bq == Bk == 128 runs the tcgen05/TMEM kernel, other block sizes the
  * mma.sync kernel. */
 FA_API fa_status fa_flex_forward(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
-                          const fa_score_rule* score_rule, float scale, void* out, float* lse,
-                          int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d,
-                          int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream);
+                                 const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype,
+                                 float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN,
+                                 int32_t d, int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream);
 
 /* Same as fa_flex_forward but always uses the mma.sync kernel (a second, independent kernel over the
  * same tables; used to cross-check the tcgen05 path). */
 FA_API fa_status fa_flex_forward_mma(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
-                              const fa_score_rule* score_rule, float scale, void* out, float* lse,
-                              int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d,
-                              int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream);
+                                     const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype,
+                                     float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN,
+                                     int32_t d, int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream);
 
 /* Paged split-KV decode ("5.1.2 FlexAttention ...", sections 3.2 "split-KV exact merge" and 5.1-5.2;
  * "FlexAttention: compiler optimisation ...", section 6; the merge law of "5 Kernels ...", section 3).
@@ -187,16 +192,18 @@ FA_API fa_status fa_flex_forward_mma(const void* q, const void* k, const void* v
  *   page_table   device int32 [Bz, max_pages]
  *   block_mask   made with Bq = 1, Bk = page, Q_LEN = 1, KV_LEN = max_pages * page, Bm in {1, Bz},
  *                Hm == 1; its rule's q_offset[b] is the query's global position (cur_pos = L_b - 1)
- *   workspace    device buffer of >= fa_decode_workspace_bytes(...) bytes, 16-byte aligned
- *   out          device bf16 [Bz, Hq, d];  lse  device fp32 [Bz, Hq]
- * Supported: d in {64, 128}; page in {32, 64, 128, 256}; 1 <= Hq/Hkv <= 16.
+ *   workspace    device buffer of >= fa_decode_workspace_bytes(...) bytes, 16-byte aligned; holds the
+ *                per-split (m, l, u) between the two kernels
+ *   out          device [Bz, Hq, d] of type out_dtype;  lse  device fp32 [Bz, Hq]
+ * Supported: d in {64, 128}; page in {32, 64, 128}; 1 <= Hq/Hkv <= 16.
  * A page id outside [0, n_pages_total) sets FA_ERR_DEVICE_CHECK in *dev_status (that page is skipped). */
 FA_API size_t fa_decode_workspace_bytes(int32_t Bz, int32_t Hq, int32_t d, int32_t max_pages, int32_t page);
 FA_API fa_status fa_flex_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
-                         int32_t n_pages_total, const fa_block_mask* block_mask, const fa_score_rule* score_rule,
-                         float scale, void* out, float* lse, int32_t Bz, int32_t Hq, int32_t Hkv, int32_t d,
-                         int32_t page, int32_t max_pages, void* workspace, size_t workspace_bytes,
-                         int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream);
+                                int32_t n_pages_total, const fa_block_mask* block_mask,
+                                const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype,
+                                float* lse, int32_t Bz, int32_t Hq, int32_t Hkv, int32_t d, int32_t page,
+                                int32_t max_pages, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                int64_t* dev_counters, fa_stream_t stream);
 
 /* Block statistics of a BlockMask ("5.1.2 FlexAttention ...", sections 2.2 and 6.3: full/partial/empty
  * counts and row lengths). dev_out: device int64[6] = {full, partial, empty, max row length (full +

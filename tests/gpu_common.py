@@ -36,7 +36,7 @@ def oracle_score(score: dict) -> dict:
     return out
 
 
-def run_prefill(w: workloads.Prefill, force_mma=False, counters=False, bq=None, bk=None):
+def run_prefill(w: workloads.Prefill, force_mma=False, counters=False, bq=None, bk=None, out_dtype=torch.float32):
     """Generate (if needed) and run create_block_mask + flex_forward; returns dict of results."""
     if w.q_bits is None:
         w.generate()
@@ -50,7 +50,8 @@ def run_prefill(w: workloads.Prefill, force_mma=False, counters=False, bq=None, 
     al, rb, sc = score_tensors(w.score, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     cnt = torch.zeros(4, dtype=torch.int64, device=dev) if counters else None
-    out, lse = fa.flex_forward(q, k, v, bm, sc, w.scale, status=status, counters=cnt, force_mma=force_mma)
+    out, lse = fa.flex_forward(q, k, v, bm, sc, w.scale, status=status, counters=cnt, force_mma=force_mma,
+                               out_dtype=out_dtype)
     st = fa.check_status(status)
     return dict(out=out, lse=lse, bm=bm, status=st, counters=cnt, keep=(al, rb, doc, q, k, v))
 
@@ -88,15 +89,28 @@ def oracle_rows(w: workloads.Prefill, pairs, rows):
     return res
 
 
-def compare(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray, what=""):
-    """Tolerance check: max/mean |O - O*| and max |LSE - LSE*| (empty rows: LSE both -inf, O both 0)."""
+def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
+    """Half a bf16 ulp at |x| (8 significant bits): the largest error of rounding x to bf16."""
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    return np.where(ax > 0, np.ldexp(1.0, (e - 8).astype(np.int64)), 0.0)
+
+
+def compare(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray, what="",
+            out_bf16: bool = False):
+    """Tolerance check: max/mean |O - O*| and max |LSE - LSE*| (empty rows: LSE both -inf, O both 0).
+
+    fp32 output: the bounds apply as stated. bf16 output: the stored value also carries the rounding of
+    the result to bf16, at most half an ulp of O*, which is added to the bound element by element (the
+    max bound alone is below that rounding for |O*| >= 4)."""
     err = np.abs(o_gpu.astype(np.float64) - o_ref)
+    slack = half_ulp_bf16(o_ref) if out_bf16 else np.zeros_like(o_ref)
     inf_ref = np.isneginf(lse_ref)
     assert np.array_equal(np.isneginf(lse_gpu), inf_ref), f"{what}: empty-row pattern differs"
     lerr = np.abs(lse_gpu[~inf_ref].astype(np.float64) - lse_ref[~inf_ref]) if (~inf_ref).any() else np.zeros(1)
     assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite output"
-    assert err.max() <= O_MAX, f"{what}: max |O err| {err.max():.3e}"
-    assert err.mean() <= O_MEAN, f"{what}: mean |O err| {err.mean():.3e}"
+    assert np.all(err <= O_MAX + slack), f"{what}: max |O err| {err.max():.3e} (excess {(err - slack).max():.3e})"
+    assert err.mean() <= O_MEAN + slack.mean(), f"{what}: mean |O err| {err.mean():.3e}"
     assert lerr.max() <= LSE_MAX, f"{what}: max |LSE err| {lerr.max():.3e}"
     return float(err.max()), float(err.mean()), float(lerr.max())
 

@@ -74,14 +74,16 @@ def test_forward_and_decode_argument_checks(lib):
     p = ctypes.c_void_p(4096)
     f = lib.fa_flex_forward
     # length mismatch with the mask is an error, never a silent trim
-    assert f(p, p, p, ctypes.byref(c), None, 0.0, p, p, 1, 2, 1, 255, 256, 128, None, None, None) == fa.ERR_SHAPE
-    assert f(p, p, p, ctypes.byref(c), None, 0.0, p, p, 1, 3, 2, 256, 256, 128, None, None, None) == fa.ERR_SHAPE
-    assert f(p, p, p, ctypes.byref(c), None, 0.0, p, p, 1, 2, 1, 256, 256, 96, None, None, None) == \
+    assert f(p, p, p, ctypes.byref(c), None, 0.0, p, 0, p, 1, 2, 1, 255, 256, 128, None, None, None) == fa.ERR_SHAPE
+    assert f(p, p, p, ctypes.byref(c), None, 0.0, p, 0, p, 1, 3, 2, 256, 256, 128, None, None, None) == fa.ERR_SHAPE
+    assert f(p, p, p, ctypes.byref(c), None, 0.0, p, 0, p, 1, 2, 1, 256, 256, 96, None, None, None) == \
         fa.ERR_UNSUPPORTED
-    assert f(ctypes.c_void_p(4097), p, p, ctypes.byref(c), None, 0.0, p, p, 1, 2, 1, 256, 256, 128, None, None,
+    assert f(ctypes.c_void_p(4097), p, p, ctypes.byref(c), None, 0.0, p, 0, p, 1, 2, 1, 256, 256, 128, None, None,
              None) == fa.ERR_INVALID_ARG                             # misaligned q
+    assert f(p, p, p, ctypes.byref(c), None, 0.0, p, 7, p, 1, 2, 1, 256, 256, 128, None, None, None) == \
+        fa.ERR_INVALID_ARG                                           # unknown output type
     assert lib.fa_decode_workspace_bytes(64, 32, 128, 256, 128) > 64 * 32 * 128 * 4
     d = lib.fa_flex_decode
     # table made for prefill (bq = 128) is rejected by decode
-    assert d(p, p, p, p, 10, ctypes.byref(c), None, 0.0, p, p, 1, 4, 2, 128, 128, 2, p, 1 << 30, None, None, None) \
-        == fa.ERR_SHAPE
+    assert d(p, p, p, p, 10, ctypes.byref(c), None, 0.0, p, 0, p, 1, 4, 2, 128, 128, 2, p, 1 << 30, None, None,
+             None) == fa.ERR_SHAPE

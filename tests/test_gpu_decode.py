@@ -14,7 +14,7 @@ from tests import gpu_common as gc
 pytestmark = pytest.mark.gpu
 
 
-def run_decode(d: workloads.Decode, table=None):
+def run_decode(d: workloads.Decode, table=None, out_dtype=torch.float32):
     dev = "cuda"
     q = workloads.bf16_torch(d.q_bits, dev)
     kp = workloads.bf16_torch(d.k_bits, dev)
@@ -26,7 +26,7 @@ def run_decode(d: workloads.Decode, table=None):
     al, rb, sc = gc.score_tensors(d.score, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     cnt = torch.zeros(4, dtype=torch.int64, device=dev)
-    out, lse = fa.flex_decode(q, kp, vp, pt, bm, sc, d.scale, status=status, counters=cnt)
+    out, lse = fa.flex_decode(q, kp, vp, pt, bm, sc, d.scale, status=status, counters=cnt, out_dtype=out_dtype)
     st = fa.check_status(status)
     return out, lse, st, cnt
 
@@ -39,18 +39,20 @@ def oracle_decode(d, requests):
                                 requests=requests, kv_len_table=d.kv_len)
 
 
-@pytest.mark.parametrize("page,g,d_,prefix", [(128, 4, 128, 0), (32, 2, 64, 0), (64, 8, 128, 40), (256, 1, 64, 0),
+@pytest.mark.parametrize("page,g,d_,prefix", [(128, 4, 128, 0), (32, 2, 64, 0), (64, 8, 128, 40), (32, 1, 64, 0),
                                               (128, 16, 128, 0)])
-def test_small_decode(page, g, d_, prefix):
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_small_decode(page, g, d_, prefix, out_dtype):
     Hkv = 2
     dec = workloads.cfg5(Bz=5, Hq=Hkv * g, Hkv=Hkv, d=d_, page=page, lo=max(1, prefix), hi=9 * page + 5,
                          prefix=prefix)
     dec.generate()
-    out, lse, st, cnt = run_decode(dec)
+    out, lse, st, cnt = run_decode(dec, out_dtype=out_dtype)
     assert st == fa.OK
     reqs = list(range(dec.Bz))
     o_ref, lse_ref = oracle_decode(dec, reqs)
-    gc.compare(out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"decode page={page} g={g}")
+    gc.compare(out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"decode page={page} g={g}",
+               out_bf16=out_dtype == torch.bfloat16)
     pages = sum(-(-int(L) // page) for L in dec.kv_lens)
     assert cnt.cpu().tolist()[3] == 2 * pages * Hkv            # each visited page read once per KV head
 

@@ -28,14 +28,15 @@ def small(name, B, Hq, Hkv, q_len, kv_len, d, bq, bk, rule, score=None, scale=No
     return w.generate()
 
 
-def full_compare(w, force_mma=False, what=""):
-    r = gc.run_prefill(w, force_mma=force_mma)
+def full_compare(w, force_mma=False, what="", out_dtype=torch.float32):
+    r = gc.run_prefill(w, force_mma=force_mma, out_dtype=out_dtype)
     assert r["status"] == fa.OK
+    assert r["out"].dtype == out_dtype
     o = r["out"].float().cpu().numpy()
     lse = r["lse"].cpu().numpy()
     qf, kf, vf = (synth.bf16_bits_to_f64(x) for x in (w.q_bits, w.k_bits, w.v_bits))
     o_ref, lse_ref = orc.attention(qf, kf, vf, w.rule, w.scale, gc.oracle_score(w.score), doc_ids=w.doc_ids)
-    return gc.compare(o, lse, o_ref, lse_ref, what or w.name), r
+    return gc.compare(o, lse, o_ref, lse_ref, what or w.name, out_bf16=out_dtype == torch.bfloat16), r
 
 
 DOC = np.repeat(np.arange(7, dtype=np.int32), [40, 3, 100, 17, 60, 9, 200])[None, :]
@@ -59,14 +60,15 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 @pytest.mark.parametrize("force_mma", [False, True])
-def test_small_cases_all_elements(case, force_mma):
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_small_cases_all_elements(case, force_mma, out_dtype):
     name, B, Hq, Hkv, ql, kl, d, bq, bk, rule, score = case
     if score is None:  # relative-bias table
         rng = np.random.default_rng(3)
         score = dict(rel_bias=(rng.standard_normal((Hq, 2 * kl - 1)) * 2).astype(np.float32))
     doc = DOC[:, :max(ql, kl)] if any(op[0] == "doc" for op in rule) else None
     w = small(name, B, Hq, Hkv, ql, kl, d, bq, bk, rule, score, doc=doc)
-    full_compare(w, force_mma=force_mma)
+    full_compare(w, force_mma=force_mma, out_dtype=out_dtype)
 
 
 def test_empty_rows_and_no_loads():
@@ -97,6 +99,7 @@ def test_cfg1_all_elements(name):
     w = workloads.cfg1().generate()
     errs, r = full_compare(w)
     errs2, _ = full_compare(w, force_mma=True)
+    errs3, _ = full_compare(w, out_dtype=torch.bfloat16)
 
 
 @pytest.mark.parametrize("name", ["cfg2", "cfg3", "cfg4"])
@@ -108,6 +111,7 @@ def test_full_size_sampled(name):
     ref = gc.oracle_rows(w, pairs, rows)
     out, lse = r["out"], r["lse"]
     for (b, h), (o_ref, lse_ref) in ref.items():
+        assert out.dtype == torch.float32
         o = out[b, h, torch.from_numpy(rows).cuda()].float().cpu().numpy()
         l = lse[b, h, torch.from_numpy(rows).cuda()].cpu().numpy()
         gc.compare(o, l, o_ref, lse_ref, f"{name} b={b} h={h}")
