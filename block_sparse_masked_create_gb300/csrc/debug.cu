@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(128) debug_tc5_gemm_kernel(const __nv_bfloat16
   __syncwarp();
   if (ok) ok = mbar_wait(&bar_mma, 0, wc);
   tc5_fence_after();
+  ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.ld below is warp-collective
   if (ok) {
     for (int c0 = 0; c0 < 128; c0 += 32) {
       uint32_t r[32];

@@ -346,8 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_ref = -INFINITY;  // reference max (log2 domain) used for P and for O
       float l = 0.f;
       bool ok = true;
+      // tcgen05.ld / st are warp-collective (.sync.aligned): every decision that guards one is made
+      // uniform across the warp (wait results with __all_sync, the O rescale with __any_sync)
       for (int j = 0; j < TT.n && ok; ++j) {
-        ok = mbar_wait(&bar_s[t], (uint32_t)(j & 1), wc);
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_s[t], (uint32_t)(j & 1), wc));
         if (!ok) break;
         tc5_fence_after();
         float x[128];
@@ -425,18 +427,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = l * alpha + rs;
         // ---- the previous P V must be complete: P buffer free, O stable
         if (j > 0) {
-          ok = mbar_wait(&bar_o[t], (uint32_t)((j - 1) & 1), wc);
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o[t], (uint32_t)((j - 1) & 1), wc));
           if (!ok) break;
           tc5_fence_after();
         }
-        if (rescale) {
+        if (__any_sync(0xFFFFFFFFu, rescale)) {
+          const float f = rescale ? alpha : 1.f;
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
             tc5_ld32(tO + c0, o);
             tc5_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
             tc5_st32(tO + c0, o);
           }
           tc5_wait_st();
@@ -451,7 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bar_p[t]);
       }
       // ---- epilogue
-      if (ok) ok = mbar_wait(&bar_o[t], (uint32_t)((TT.n - 1) & 1), wc);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o[t], (uint32_t)((TT.n - 1) & 1), wc));
       tc5_fence_after();
       if (ok) {
         const bool empty = m_ref == -INFINITY;
