@@ -83,6 +83,18 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.samples.append([x.strip() for x in line.split(",")])
 
+    def busy_until_sampled(self, work, n=3, max_s=8.0):
+        """Run `work` (GPU work + sync) until the sampler has seen n samples, so that the timed region
+        that follows sits inside a sampled window under the same load."""
+        t0 = time.perf_counter()
+        while self.proc and len(self.samples) < n and time.perf_counter() - t0 < max_s:
+            work()
+
+    def busy_for(self, work, seconds):
+        t0 = time.perf_counter()
+        while self.proc and time.perf_counter() - t0 < seconds:
+            work()
+
     def __exit__(self, *a):
         if self.proc:
             self.proc.terminate()
@@ -104,7 +116,8 @@ class ClockSampler:
             except Exception:
                 pass
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "200 ms samples while the step runs back to back, before, during "
+                                              "and after the timed region"}
 
 
 # ------------------------------------------------------------------------------------------------------
@@ -234,7 +247,17 @@ def ours(args, rank, world, local_rank):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    def busy():
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+
     with ClockSampler(local_rank) as clk:
+        clk.busy_until_sampled(busy)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        n_before = len(clk.samples)
         t0 = time.perf_counter()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
@@ -248,6 +271,7 @@ def ours(args, rank, world, local_rank):
         end.record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+        clk.busy_for(busy, 0.5)
     if dist:
         dist.barrier()
     ms = start.elapsed_time(end)

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kDecWarps * 32)
   const float slope_b = (a.score.alibi && rb < g) ? __ldg(a.score.alibi + hk * g + rb) : 0.f;
   const float scale_log2 = a.scale * kLog2e;
 
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f, le_a = 0.f, le_b = 0.f;
   float o[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kDecWarps * 32)
       m_a = mn_a;
       m_b = mn_b;
       uint32_t pf[2][4];
-      float ps_a = 0.f, ps_b = 0.f;
+      float ps_a = 0.f, ps_b = 0.f, pe_a = 0.f, pe_b = 0.f;
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         const float p0 = ex2_approx(sc[nt][0] - ref_a), p1 = ex2_approx(sc[nt][1] - ref_a);
@@ -234,11 +234,15 @@ __global__ void __launch_bounds__(kDecWarps * 32)
         const uint32_t pa = pack_bf16x2(p0, p1), pb = pack_bf16x2(p2, p3);
         pf[nt >> 1][(nt & 1) * 2 + 0] = pa;
         pf[nt >> 1][(nt & 1) * 2 + 1] = pb;
-        ps_a += bf16x2_sum(pa);  // row sums of the rounded P the product uses
+        ps_a += bf16x2_sum(pa);  // sums of the rounded P the product uses (normalise O)
         ps_b += bf16x2_sum(pb);
+        pe_a += p0 + p1;         // sums of the unrounded P (LSE)
+        pe_b += p2 + p3;
       }
       l_a = l_a * al_a + ps_a;
       l_b = l_b * al_b + ps_b;
+      le_a = le_a * al_a + pe_a;
+      le_b = le_b * al_b + pe_b;
 #pragma unroll
       for (int dt = 0; dt < D / 8; ++dt) {
         o[dt][0] *= al_a;
@@ -281,9 +285,14 @@ __global__ void __launch_bounds__(kDecWarps * 32)
   l_a += __shfl_xor_sync(0xFFFFFFFFu, l_a, 2);
   l_b += __shfl_xor_sync(0xFFFFFFFFu, l_b, 1);
   l_b += __shfl_xor_sync(0xFFFFFFFFu, l_b, 2);
+  le_a += __shfl_xor_sync(0xFFFFFFFFu, le_a, 1);
+  le_a += __shfl_xor_sync(0xFFFFFFFFu, le_a, 2);
+  le_b += __shfl_xor_sync(0xFFFFFFFFu, le_b, 1);
+  le_b += __shfl_xor_sync(0xFFFFFFFFu, le_b, 2);
   float* sO = reinterpret_cast<float*>(smem);             // [4][16][D]
   float* sM = sO + kDecWarps * 16 * D;                    // [4][16]
   float* sL = sM + kDecWarps * 16;                        // [4][16]
+  float* sLe = sL + kDecWarps * 16;                       // [4][16]
 #pragma unroll
   for (int dt = 0; dt < D / 8; ++dt) {
     const int col = dt * 8 + (lane & 3) * 2;
@@ -297,6 +306,8 @@ __global__ void __launch_bounds__(kDecWarps * 32)
     sM[warp * 16 + rb] = m_b;
     sL[warp * 16 + ra] = l_a;
     sL[warp * 16 + rb] = l_b;
+    sLe[warp * 16 + ra] = le_a;
+    sLe[warp * 16 + rb] = le_b;
   }
   __syncthreads();
   const size_t ns = (size_t)a.n_splits;
@@ -306,12 +317,13 @@ __global__ void __launch_bounds__(kDecWarps * 32)
 #pragma unroll
     for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, sM[w * 16 + row]);
     const float ref = mm == -INFINITY ? 0.f : mm;
-    float u = 0.f, l = 0.f;
+    float u = 0.f, l = 0.f, le = 0.f;
 #pragma unroll
     for (int w = 0; w < kDecWarps; ++w) {
       const float wt = ex2_approx(sM[w * 16 + row] - ref);
       u += wt * sO[(w * 16 + row) * D + col];
       l += wt * sL[w * 16 + row];
+      le += wt * sLe[w * 16 + row];
     }
     const size_t hq = (size_t)hk * g + row;
     const size_t slot = ((size_t)b * a.Hq + hq) * ns + s;
@@ -319,6 +331,7 @@ __global__ void __launch_bounds__(kDecWarps * 32)
     if (col == 0) {
       a.ws_m[slot] = mm;
       a.ws_l[slot] = l;
+      a.ws_le[slot] = le;
     }
   }
 }
@@ -335,8 +348,12 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
   float mm = -INFINITY;
   for (int s = 0; s < ns; ++s) mm = fmaxf(mm, a.ws_m[base + s]);
   const float ref = mm == -INFINITY ? 0.f : mm;
-  float l = 0.f;
-  for (int s = 0; s < ns; ++s) l += ex2_approx(a.ws_m[base + s] - ref) * a.ws_l[base + s];
+  float l = 0.f, le = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float wt = ex2_approx(a.ws_m[base + s] - ref);
+    l += wt * a.ws_l[base + s];
+    le += wt * a.ws_le[base + s];
+  }
   const bool empty = mm == -INFINITY;
   const float inv = empty ? 0.f : 1.f / l;
   for (int col = threadIdx.x; col < D; col += blockDim.x) {
@@ -347,7 +364,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
     else
       reinterpret_cast<__nv_bfloat16*>(a.out)[obase + col] = __float2bfloat16_rn(u * inv);
   }
-  if (threadIdx.x == 0) a.lse[(size_t)b * a.Hq + hq] = empty ? -INFINITY : (mm + __log2f(l)) * kLn2;
+  if (threadIdx.x == 0) a.lse[(size_t)b * a.Hq + hq] = empty ? -INFINITY : (mm + __log2f(le)) * kLn2;
 }
 
 template <int D>

@@ -374,7 +374,7 @@ size_t fa_decode_workspace_bytes(int32_t Bz, int32_t Hq, int32_t d, int32_t max_
   const int ps = decode_pages_per_split(page, max_pages);
   const size_t ns = (size_t)((max_pages + ps - 1) / ps);
   const size_t slots = (size_t)Bz * Hq * ns;
-  return align256(slots * 4) * 2 + align256(slots * (size_t)d * 4);
+  return align256(slots * 4) * 3 + align256(slots * (size_t)d * 4);
 }
 
 fa_status fa_flex_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
@@ -424,7 +424,8 @@ fa_status fa_flex_decode(const void* q, const void* k_pages, const void* v_pages
   uint8_t* w = static_cast<uint8_t*>(workspace);
   a.ws_m = reinterpret_cast<float*>(w);
   a.ws_l = reinterpret_cast<float*>(w + align256(slots * 4));
-  a.ws_u = reinterpret_cast<float*>(w + 2 * align256(slots * 4));
+  a.ws_le = reinterpret_cast<float*>(w + 2 * align256(slots * 4));
+  a.ws_u = reinterpret_cast<float*>(w + 3 * align256(slots * 4));
   a.status = dev_status;
   a.counters = dev_counters;
   a.timeout_ns = g_timeout_ns.load();

@@ -70,7 +70,8 @@ struct DecArgs {
   DevScore score;
   DevMask mask;
   float* ws_m;      // [Bz, Hq, n_splits]
-  float* ws_l;      // [Bz, Hq, n_splits]
+  float* ws_l;      // [Bz, Hq, n_splits]  sum of the bf16-rounded P (normalises O)
+  float* ws_le;     // [Bz, Hq, n_splits]  sum of the unrounded P (LSE)
   float* ws_u;      // [Bz, Hq, n_splits, d]
   int32_t pages_per_split, n_splits;
   int32_t* status;

@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(MmaCfg<D, BQ, BK>::kThreads)
   cp_async_commit();
 
   // softmax state per row (log2 domain)
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f, le_a = 0.f, le_b = 0.f;
   float o[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -217,22 +217,26 @@ __global__ void __launch_bounds__(MmaCfg<D, BQ, BK>::kThreads)
     const float al_a = ex2_approx(m_a - ref_a), al_b = ex2_approx(m_b - ref_b);  // 0 when m was -inf
     m_a = mn_a;
     m_b = mn_b;
-    float ps_a = 0.f, ps_b = 0.f;
+    float ps_a = 0.f, ps_b = 0.f, pe_a = 0.f, pe_b = 0.f;
     uint32_t pf[BK / 16][4];
 #pragma unroll
     for (int nt = 0; nt < BK / 8; ++nt) {
       const float p0 = ex2_approx(s[nt][0] - ref_a), p1 = ex2_approx(s[nt][1] - ref_a);
       const float p2 = ex2_approx(s[nt][2] - ref_b), p3 = ex2_approx(s[nt][3] - ref_b);
-      // C-fragment of n-tiles (2k, 2k+1) -> A-fragment of k-step k; the row sums use the rounded P that
-      // the P V product sees, so O is an exact convex combination of the V rows
+      // C-fragment of n-tiles (2k, 2k+1) -> A-fragment of k-step k. Two row sums: of the rounded P the
+      // P V product sees (normalises O: an exact convex combination of V rows) and of the unrounded P (LSE)
       const uint32_t pa = pack_bf16x2(p0, p1), pb = pack_bf16x2(p2, p3);
       pf[nt >> 1][(nt & 1) * 2 + 0] = pa;
       pf[nt >> 1][(nt & 1) * 2 + 1] = pb;
       ps_a += bf16x2_sum(pa);
       ps_b += bf16x2_sum(pb);
+      pe_a += p0 + p1;
+      pe_b += p2 + p3;
     }
     l_a = l_a * al_a + ps_a;
     l_b = l_b * al_b + ps_b;
+    le_a = le_a * al_a + pe_a;
+    le_b = le_b * al_b + pe_b;
 #pragma unroll
     for (int dt = 0; dt < D / 8; ++dt) {
       o[dt][0] *= al_a;
@@ -260,11 +264,15 @@ __global__ void __launch_bounds__(MmaCfg<D, BQ, BK>::kThreads)
   l_a += __shfl_xor_sync(0xFFFFFFFFu, l_a, 2);
   l_b += __shfl_xor_sync(0xFFFFFFFFu, l_b, 1);
   l_b += __shfl_xor_sync(0xFFFFFFFFu, l_b, 2);
+  le_a += __shfl_xor_sync(0xFFFFFFFFu, le_a, 1);
+  le_a += __shfl_xor_sync(0xFFFFFFFFu, le_a, 2);
+  le_b += __shfl_xor_sync(0xFFFFFFFFu, le_b, 1);
+  le_b += __shfl_xor_sync(0xFFFFFFFFu, le_b, 2);
   const bool emp_a = m_a == -INFINITY, emp_b = m_b == -INFINITY;
   const float inv_a = emp_a ? 0.f : 1.f / l_a, inv_b = emp_b ? 0.f : 1.f / l_b;
   if ((lane & 3) == 0) {
-    if (row_a < a.q_len) Lg[row_a] = emp_a ? -INFINITY : (m_a + __log2f(l_a)) * kLn2;
-    if (row_b < a.q_len) Lg[row_b] = emp_b ? -INFINITY : (m_b + __log2f(l_b)) * kLn2;
+    if (row_a < a.q_len) Lg[row_a] = emp_a ? -INFINITY : (m_a + __log2f(le_a)) * kLn2;
+    if (row_b < a.q_len) Lg[row_b] = emp_b ? -INFINITY : (m_b + __log2f(le_b)) * kLn2;
   }
   if (a.out_f32) {
     float* Of = reinterpret_cast<float*>(a.out) + ((size_t)b * a.Hq + h) * a.q_len * D;

@@ -329,10 +329,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* Lg = a.lse + ((size_t)b * a.Hq + TT.h) * a.q_len;
     if (TT.valid && TT.n == 0) {
       // empty query block: O = 0, LSE = -inf, nothing loaded
-      __nv_bfloat16* Og = reinterpret_cast<__nv_bfloat16*>(a.out) + (((size_t)b * a.Hq + TT.h) * a.q_len) * D;
+      const int row_bytes = D * (a.out_f32 ? 4 : 2);
+      uint8_t* Ob = reinterpret_cast<uint8_t*>(a.out) + (((size_t)b * a.Hq + TT.h) * a.q_len) * row_bytes;
       if (q_row < a.q_len) {
-        uint4 z = make_uint4(0, 0, 0, 0);
-        for (int c16 = 0; c16 < D / 8; ++c16) *reinterpret_cast<uint4*>(Og + (size_t)q_row * D + c16 * 8) = z;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int c16 = 0; c16 < row_bytes / 16; ++c16)
+          *reinterpret_cast<uint4*>(Ob + (size_t)q_row * row_bytes + c16 * 16) = z;
         Lg[q_row] = -INFINITY;
       }
     } else if (TT.valid) {
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float slope2 = 0.f;
       if (SK == SK_ALIBI || SK == SK_GENERIC) slope2 = a.score.alibi ? __ldg(a.score.alibi + TT.h) * kLog2e : 0.f;
       float m_ref = -INFINITY;  // reference max (log2 domain) used for P and for O
-      float l = 0.f;
+      float l = 0.f, le = 0.f;
       bool ok = true;
       // tcgen05.ld / st are warp-collective (.sync.aligned): every decision that guards one is made
       // uniform across the warp (wait results with __all_sync, the O rescale with __any_sync)
@@ -416,15 +418,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = mb;
         }
         const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-        float rs = 0.f;
+        // two row sums: of the bf16-rounded P the product uses (normalises O, so O is an exact convex
+        // combination of V rows) and of the unrounded P (for the LSE)
+        float rs = 0.f, rse = 0.f;
         uint32_t pk[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           const float p0 = ex2_approx(x[2 * i] - mr), p1 = ex2_approx(x[2 * i + 1] - mr);
           pk[i] = pack_bf16x2(p0, p1);
-          rs += bf16x2_sum(pk[i]);  // row sum of the rounded P the product uses
+          rs += bf16x2_sum(pk[i]);
+          rse += p0 + p1;
         }
         l = l * alpha + rs;
+        le = le * alpha + rse;
         // ---- the previous P V must be complete: P buffer free, O stable
         if (j > 0) {
           ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o[t], (uint32_t)((j - 1) & 1), wc));
@@ -494,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (q_row < a.q_len) Lg[q_row] = empty ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
+        if (q_row < a.q_len) Lg[q_row] = empty ? -INFINITY : (m_ref + __log2f(le)) * kLn2;
       }
       // every thread of the warpgroup reaches this barrier (ok or not); the store runs only if no role
       // gave up (a failed wait always sets the CTA's abort flag)
