@@ -120,7 +120,11 @@ def test_full_size_sampled(name):
     c = r["counters"].cpu().tolist()
     heads = w.B * w.Hq // (r["bm"].c.Bm * r["bm"].c.Hm)
     assert c[1] == st[0] * heads and c[2] == st[1] * heads
-    assert c[3] == 2 * (c[1] + c[2])
+    # one K and one V load per visited block; the tcgen05 kernel shares them between the two query
+    # tiles of a CTA when both heads read the same KV head through the same mask row (GQA)
+    g = w.Hq // w.Hkv
+    shared = w.bq == 128 and w.bk == 128 and g >= 2 and w.Hq % 2 == 0 and r["bm"].c.Hm == 1
+    assert c[3] == (1 if shared else 2) * (c[1] + c[2])
     assert np.all(np.isfinite(out.float().cpu().numpy()))
 
 
