@@ -8,21 +8,22 @@
 // O = acc / l and LSE = m + ln l, an empty row giving O = 0, LSE = -inf.
 //
 // How (one CTA = two 128-row query tiles of sibling heads of the same query block, 10 warps):
-//   warps 0-3 / 4-7  softmax warpgroups of tile 0 / tile 1: S from TMEM to registers (one row per
-//                    thread), score rule, mask, row max, exp2, row sum; P as bf16 into shared memory in
-//                    the 128-byte-swizzled K-major layout the MMA reads; rescale of the O accumulator in
-//                    TMEM only when the running max grows by more than 2^8 (the result is exact for any
-//                    reference max; the bound keeps P <= 256); epilogue O / l -> bf16 -> TMA store.
+//   warps 0-3 / 4-7  softmax warpgroups of tile 0 / tile 1 (TMEM lane = query row = thread). Per block:
+//                    S from TMEM to registers, "S free" signal, score rule, mask, row max (3-input max
+//                    tree), P = 2^(x - m) with packed fp32x2 FMAs, row sums, P as bf16 into shared
+//                    memory (128-byte swizzled K-major layout), "P ready" signal. The O accumulator is
+//                    rescaled in TMEM only when the running max grows by more than 2^8 (exact for any
+//                    reference max; the bound keeps P <= 256). Epilogue O / l -> TMA store.
 //   warp 8           TMA producer: Q tiles, then K / V tiles of the visited blocks only (an empty block
 //                    issues no load) into a ring of shared-memory slots, in exactly the order the MMA
 //                    warp consumes them. Sibling query heads of one KV head with the same mask row share
 //                    each K / V load.
-//   warp 9           allocates TMEM (512 columns: S and O of both tiles) and issues every tcgen05.mma from
-//                    one thread: S_t = Q_t K^T (A, B K-major), O_t += P_t V (A K-major, B = V MN-major);
-//                    completion is signalled with tcgen05.commit on mbarriers.
-// The two tiles ping-pong: while one warpgroup works on its softmax, the tensor core runs the other
-// tile's MMAs. Every wait is bounded (an abort flag stops all roles; copies and MMAs in flight are
-// drained before tensor memory is freed and the CTA exits).
+//   warp 9           allocates TMEM (S and O of both tiles: 512 columns) and issues every tcgen05.mma from
+//                    one thread. S_t(j+1) = Q_t K(j+1)^T is issued as soon as the softmax has read S_t(j)
+//                    (so it overlaps the softmax of block j), O_t += P_t(j) V(j) when P_t(j) is ready.
+// Two tiles in flight keep the tensor core busy while each warpgroup runs its softmax. Every wait is
+// bounded (an abort flag stops all roles; copies and MMAs in flight are drained before tensor memory is
+// freed and the CTA exits).
 #include <cstring>
 
 #include "fa_launch.h"
@@ -56,7 +57,6 @@ struct Tc5Cfg {
 
 struct Tc5Params {
   FwdArgs a;
-  int n_pairs, heads_per_pair_groups;  // pairs = B * nq * ceil(Hq / 2)
 };
 
 // byte offset of 16-byte chunk c16 of row `row` in a [128][D] tile stored as D/64 sub-tiles [128][64]
@@ -68,11 +68,28 @@ __device__ __forceinline__ uint32_t tile_off(int row, int c16) {
 struct Tile {
   int valid;     // a tile exists (Hq may be odd)
   int h, hk;     // query head, KV head
-  int n_full, n_part, n;
+  int n_full, n;
   const int32_t* full_idx;
   const int32_t* part_idx;
-  __device__ __forceinline__ int col(int j) const { return j < n_full ? __ldg(full_idx + j) : __ldg(part_idx + j - n_full); }
+  __device__ __forceinline__ int col(int j) const {
+    return j < n_full ? __ldg(full_idx + j) : __ldg(part_idx + j - n_full);
+  }
 };
+
+__device__ __forceinline__ Tile make_tile(const FwdArgs& a, int b, int h, int r) {
+  const DevMask& M = a.mask;
+  Tile T;
+  T.valid = h < a.Hq;
+  T.h = T.valid ? h : 0;
+  T.hk = T.h / (a.Hq / a.Hkv);
+  const int bm = M.Bm > 1 ? b : 0, hm = M.Hm > 1 ? T.h : 0;
+  const size_t mrow = ((size_t)bm * M.Hm + hm) * M.nq + r;
+  T.n_full = T.valid ? __ldg(M.full_kv_num + mrow) : 0;
+  T.n = T.valid ? T.n_full + __ldg(M.kv_num + mrow) : 0;
+  T.full_idx = M.full_kv_idx + mrow * M.nk;
+  T.part_idx = M.kv_idx + mrow * M.nk;
+  return T;
+}
 
 template <int D, int SK>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -84,7 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const FwdArgs& a = P.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q[2], bar_s[2], bar_p[2], bar_o[2], bar_full[NST], bar_empty[NST], bar_drain;
+  __shared__ uint64_t bar_q[2], bar_s[2], bar_sfree[2], bar_p[2], bar_o[2], bar_full[NST], bar_empty[NST],
+      bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int32_t s_abort;
 
@@ -98,35 +116,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   p /= HP;
   const int b = p % a.B;
   const int r = M.nq - 1 - p / a.B;
-  const int g = a.Hq / a.Hkv;
-  Tile T[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int h = 2 * hp + t;
-    T[t].valid = h < a.Hq;
-    T[t].h = T[t].valid ? h : 0;
-    T[t].hk = T[t].h / g;
-    const int bm = M.Bm > 1 ? b : 0, hm = M.Hm > 1 ? T[t].h : 0;
-    const size_t mrow = ((size_t)bm * M.Hm + hm) * M.nq + r;
-    T[t].n_full = T[t].valid ? __ldg(M.full_kv_num + mrow) : 0;
-    T[t].n_part = T[t].valid ? __ldg(M.kv_num + mrow) : 0;
-    T[t].n = T[t].n_full + T[t].n_part;
-    T[t].full_idx = M.full_kv_idx + mrow * M.nk;
-    T[t].part_idx = M.kv_idx + mrow * M.nk;
-  }
+  const Tile T0 = make_tile(a, b, 2 * hp, r);
+  const Tile T1 = make_tile(a, b, 2 * hp + 1, r);
   // sibling heads of one KV head with the same mask row share K / V loads
-  const bool shared_kv = T[1].valid && T[0].hk == T[1].hk && T[0].n > 0 && M.Hm == 1;
-  const int nmax = max(T[0].n, T[1].n);
+  const bool shared_kv = T1.valid && T0.hk == T1.hk && T0.n > 0 && M.Hm == 1;
+  const int nmax = max(T0.n, T1.n);
 
-  uint8_t* sQ[2] = {smem, smem + C::kQBytes};
-  uint8_t* sP[2] = {smem + C::kOffP, smem + C::kOffP + C::kPBytes};
+  uint8_t* sQ0 = smem;
+  uint8_t* sQ1 = smem + C::kQBytes;
+  uint8_t* sP0 = smem + C::kOffP;
+  uint8_t* sP1 = smem + C::kOffP + C::kPBytes;
   uint8_t* sRing = smem + C::kOffRing;
 
   if (tid == 0) {
     s_abort = 0;
+#pragma unroll
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_q[t], 1);
       mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_sfree[t], 128);
       mbar_init(&bar_p[t], 128);
       mbar_init(&bar_o[t], 1);
     }
@@ -155,57 +163,64 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kLoadWarp) {
     // =============================== TMA producer ===============================
+    // load order == consumption order of the MMA warp:
+    //   separate K/V: K0(0) K1(0), then per j: K0(j+1) K1(j+1) V0(j) V1(j)   (each only if it exists)
+    //   shared K/V:   K(0), then per j: K(j+1) V(j)
     if (lane == 0) {
       if (a.counters) {
         unsigned long long* cnt = reinterpret_cast<unsigned long long*>(a.counters);
-        const int vis = T[0].n + T[1].n;
-        atomicAdd(cnt + 0, (unsigned long long)(T[0].valid + T[1].valid));
-        atomicAdd(cnt + 1, (unsigned long long)(T[0].n_full + T[1].n_full));
-        atomicAdd(cnt + 2, (unsigned long long)(T[0].n_part + T[1].n_part));
+        const int vis = T0.n + T1.n;
+        atomicAdd(cnt + 0, (unsigned long long)(T0.valid + T1.valid));
+        atomicAdd(cnt + 1, (unsigned long long)(T0.n_full + T1.n_full));
+        atomicAdd(cnt + 2, (unsigned long long)(T0.n - T0.n_full + T1.n - T1.n_full));
         atomicAdd(cnt + 3, (unsigned long long)(shared_kv ? vis : 2 * vis));
       }
-      for (int t = 0; t < 2; ++t) {
-        if (T[t].n == 0) continue;
-        mbar_arrive_expect_tx(&bar_q[t], C::kQBytes);
+      if (T0.n > 0) {
+        mbar_arrive_expect_tx(&bar_q[0], C::kQBytes);
 #pragma unroll
-        for (int x = 0; x < D / 64; ++x)
-          tma_load_3d(sQ[t] + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T[t].h, &bar_q[t]);
+        for (int x = 0; x < D / 64; ++x) tma_load_3d(sQ0 + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T0.h, &bar_q[0]);
+      }
+      if (T1.n > 0) {
+        mbar_arrive_expect_tx(&bar_q[1], C::kQBytes);
+#pragma unroll
+        for (int x = 0; x < D / 64; ++x) tma_load_3d(sQ1 + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T1.h, &bar_q[1]);
       }
       int issued = 0;
       bool ok = true;
-      auto load = [&](int t, bool is_v, int j) -> bool {
+      auto load = [&](const Tile& T, bool is_v, int j) -> bool {
         const int s = issued % NST;
         if (issued >= NST && !mbar_wait(&bar_empty[s], (uint32_t)(((issued / NST) - 1) & 1), wc)) return false;
-        const int c = T[t].col(j);
+        const int c = T.col(j);
         uint8_t* dst = sRing + s * C::kSlotBytes;
         mbar_arrive_expect_tx(&bar_full[s], C::kSlotBytes);
 #pragma unroll
         for (int x = 0; x < D / 64; ++x)
-          tma_load_3d(dst + x * 16384, is_v ? &tmV : &tmK, x * 64, c * 128, b * a.Hkv + T[t].hk, &bar_full[s]);
+          tma_load_3d(dst + x * 16384, is_v ? &tmV : &tmK, x * 64, c * 128, b * a.Hkv + T.hk, &bar_full[s]);
         ++issued;
         return true;
       };
       if (shared_kv) {
-        ok = load(0, false, 0);
-        for (int j = 1; j <= T[0].n && ok; ++j) {
-          ok = load(0, true, j - 1);
-          if (ok && j < T[0].n) ok = load(0, false, j);
+        ok = load(T0, false, 0);
+        for (int j = 0; j < T0.n && ok; ++j) {
+          if (j + 1 < T0.n) ok = load(T0, false, j + 1);
+          if (ok) ok = load(T0, true, j);
         }
       } else {
-        for (int t = 0; t < 2 && ok; ++t)
-          if (T[t].n > 0) ok = load(t, false, 0);
-        for (int j = 1; j <= nmax && ok; ++j)
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j - 1 < T[t].n) ok = load(t, true, j - 1);
-            if (ok && j < T[t].n) ok = load(t, false, j);
-          }
+        if (T0.n > 0) ok = load(T0, false, 0);
+        if (ok && T1.n > 0) ok = load(T1, false, 0);
+        for (int j = 0; j < nmax && ok; ++j) {
+          if (j + 1 < T0.n) ok = load(T0, false, j + 1);
+          if (ok && j + 1 < T1.n) ok = load(T1, false, j + 1);
+          if (ok && j < T0.n) ok = load(T0, true, j);
+          if (ok && j < T1.n) ok = load(T1, true, j);
+        }
       }
       if (!ok || *wc.abort) {
         // drain: the last NST issued copies may still be landing in shared memory
         for (int i = max(0, issued - NST); i < issued; ++i)
           mbar_wait_drain(&bar_full[i % NST], (uint32_t)((i / NST) & 1), a.timeout_ns);
-        for (int t = 0; t < 2; ++t)
-          if (T[t].n > 0) mbar_wait_drain(&bar_q[t], 0, a.timeout_ns);
+        if (T0.n > 0) mbar_wait_drain(&bar_q[0], 0, a.timeout_ns);
+        if (T1.n > 0) mbar_wait_drain(&bar_q[1], 0, a.timeout_ns);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -215,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
       int consumed = 0;
       bool ok = true;
-      for (int t = 0; t < 2 && ok; ++t)
-        if (T[t].n > 0) ok = mbar_wait(&bar_q[t], 0, wc);
+      if (T0.n > 0) ok = mbar_wait(&bar_q[0], 0, wc);
+      if (ok && T1.n > 0) ok = mbar_wait(&bar_q[1], 0, wc);
       tc5_fence_after();
       auto take = [&]() -> int {  // wait for the next ring slot in load order
         const int s = consumed % NST;
@@ -226,89 +241,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         return s;
       };
       auto mma_qk = [&](int t, int s) {
-        const uint32_t qa = smem_u32(sQ[t]), ka = smem_u32(sRing + s * C::kSlotBytes);
+        const uint32_t qa = smem_u32(t ? sQ1 : sQ0), ka = smem_u32(sRing + s * C::kSlotBytes);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          tc5_mma_ss(tmem + C::col_s(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_qk,
-                     ks > 0 ? 1u : 0u);
+          tc5_mma_ss(tmem + C::col_s(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                     idesc_qk, ks > 0 ? 1u : 0u);
         }
+        tc5_commit(&bar_s[t]);
       };
       auto mma_pv = [&](int t, int s, bool acc) {
-        const uint32_t pa = smem_u32(sP[t]), va = smem_u32(sRing + s * C::kSlotBytes);
+        const uint32_t pa = smem_u32(t ? sP1 : sP0), va = smem_u32(sRing + s * C::kSlotBytes);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t offp = (ks >> 2) * 16384 + (ks & 3) * 32;
           tc5_mma_ss(tmem + C::col_o(t), sdesc_sw128(pa + offp, 16, 1024),
                      sdesc_sw128(va + ks * 2048, 128 * 128, 1024), idesc_pv, (acc || ks > 0) ? 1u : 0u);
         }
+        tc5_commit(&bar_o[t]);
+      };
+      auto wait_p = [&](int t, int j) -> bool {
+        if (!mbar_wait(&bar_p[t], (uint32_t)(j & 1), wc)) return false;
+        tc5_fence_after();
+        return true;
+      };
+      auto wait_sfree = [&](int t, int j) -> bool {
+        if (!mbar_wait(&bar_sfree[t], (uint32_t)(j & 1), wc)) return false;
+        tc5_fence_after();
+        return true;
       };
       if (ok) {
         if (shared_kv) {
-          const int n = T[0].n;
+          const int n = T0.n;
           int sk = take();
           ok = sk >= 0;
           if (ok) {
             mma_qk(0, sk);
-            tc5_commit(&bar_s[0]);
             mma_qk(1, sk);
-            tc5_commit(&bar_s[1]);
             tc5_commit(&bar_empty[sk]);
           }
-          for (int j = 1; j <= n && ok; ++j) {
-            ok = mbar_wait(&bar_p[0], (uint32_t)((j - 1) & 1), wc);
-            if (!ok) break;
-            tc5_fence_after();
+          for (int j = 0; j < n && ok; ++j) {
+            if (j + 1 < n) {
+              if (!(ok = wait_sfree(0, j))) break;
+              if ((sk = take()) < 0) { ok = false; break; }
+              mma_qk(0, sk);
+              if (!(ok = wait_sfree(1, j))) break;
+              mma_qk(1, sk);
+              tc5_commit(&bar_empty[sk]);
+            }
+            if (!(ok = wait_p(0, j))) break;
             const int sv = take();
             if (sv < 0) { ok = false; break; }
-            mma_pv(0, sv, j > 1);
-            tc5_commit(&bar_o[0]);
-            int sk2 = -1;
-            if (j < n) {
-              sk2 = take();
-              if (sk2 < 0) { ok = false; break; }
-              mma_qk(0, sk2);
-              tc5_commit(&bar_s[0]);
-            }
-            ok = mbar_wait(&bar_p[1], (uint32_t)((j - 1) & 1), wc);
-            if (!ok) break;
-            tc5_fence_after();
-            mma_pv(1, sv, j > 1);
-            tc5_commit(&bar_o[1]);
+            mma_pv(0, sv, j > 0);
+            if (!(ok = wait_p(1, j))) break;
+            mma_pv(1, sv, j > 0);
             tc5_commit(&bar_empty[sv]);
-            if (j < n) {
-              mma_qk(1, sk2);
-              tc5_commit(&bar_s[1]);
-              tc5_commit(&bar_empty[sk2]);
-            }
           }
         } else {
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (T[t].n == 0) continue;
+          const Tile* TT[2] = {&T0, &T1};
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok || TT[t]->n == 0) continue;
             const int s = take();
             if (s < 0) { ok = false; break; }
             mma_qk(t, s);
-            tc5_commit(&bar_s[t]);
             tc5_commit(&bar_empty[s]);
           }
-          for (int j = 1; j <= nmax && ok; ++j) {
-            for (int t = 0; t < 2 && ok; ++t) {
-              if (j - 1 >= T[t].n) continue;
-              ok = mbar_wait(&bar_p[t], (uint32_t)((j - 1) & 1), wc);
-              if (!ok) break;
-              tc5_fence_after();
-              const int sv = take();
-              if (sv < 0) { ok = false; break; }
-              mma_pv(t, sv, j > 1);
-              tc5_commit(&bar_o[t]);
-              tc5_commit(&bar_empty[sv]);
-              if (j < T[t].n) {
-                const int sk = take();
-                if (sk < 0) { ok = false; break; }
-                mma_qk(t, sk);
-                tc5_commit(&bar_s[t]);
-                tc5_commit(&bar_empty[sk]);
-              }
+          for (int j = 0; j < nmax && ok; ++j) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (!ok || j + 1 >= TT[t]->n) continue;
+              if (!(ok = wait_sfree(t, j))) break;
+              const int s = take();
+              if (s < 0) { ok = false; break; }
+              mma_qk(t, s);
+              tc5_commit(&bar_empty[s]);
+            }
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (!ok || j >= TT[t]->n) continue;
+              if (!(ok = wait_p(t, j))) break;
+              const int s = take();
+              if (s < 0) { ok = false; break; }
+              mma_pv(t, s, j > 0);
+              tc5_commit(&bar_empty[s]);
             }
           }
         }
@@ -321,7 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =============================== softmax warpgroups ===============================
     const int t = warp >> 2;                 // tile of this warpgroup
     const int row = (warp & 3) * 32 + lane;  // TMEM lane == query row in the tile
-    const Tile& TT = T[t];
+    const Tile TT = t ? T1 : T0;
+    uint8_t* const sQt = t ? sQ1 : sQ0;
+    uint8_t* const sPt = t ? sP1 : sP0;
     const int q_row = r * 128 + row;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::col_s(t);
@@ -358,17 +376,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 32) tc5_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&x[c0]));
         tc5_wait_ld();
+        // S is in registers: the MMA warp may overwrite it with the next block's scores
+        tc5_fence_before();
+        mbar_arrive(&bar_sfree[t]);
         const bool partial = j >= TT.n_full;
-        const int c = TT.col(j);
+        const bool need_col = partial || SK != SK_NONE;
+        const int c = need_col ? TT.col(j) : 0;
         const int64_t j0 = (int64_t)c * 128;
-        // ---- scale + score rule, in the log2 domain
+        // ---- score rule (log2 domain); SK_NONE defers the scale into the exponent's FMA
+        float mult = 1.f;
         if (SK == SK_NONE) {
-#pragma unroll
-          for (int i = 0; i < 128; ++i) x[i] *= sl2;
+          mult = sl2;
         } else if (SK == SK_ALIBI) {
           const float base = -slope2 * (float)(ig - j0);  // bias at column 0 (log2 units)
+          const uint64_t s2 = f2_pack(sl2, sl2), sp2 = f2_pack(slope2, slope2), b2 = f2_pack(base, base);
 #pragma unroll
-          for (int i = 0; i < 128; ++i) x[i] = fmaf(x[i], sl2, fmaf(slope2, (float)i, base));
+          for (int i = 0; i < 128; i += 2) {
+            const uint64_t bias = f2_fma(sp2, f2_pack((float)i, (float)(i + 1)), b2);
+            f2_unpack(f2_fma(f2_pack(x[i], x[i + 1]), s2, bias), x[i], x[i + 1]);
+          }
         } else if (SK == SK_SOFTCAP) {
 #pragma unroll
           for (int i = 0; i < 128; ++i)
@@ -406,9 +432,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) x[k * 32 + i] = ((wd >> i) & 1u) ? x[k * 32 + i] : -INFINITY;
           }
         }
-        float mb = -INFINITY;
+        // ---- row max: 8 independent 3-input max chains
+        float mxk[8];
 #pragma unroll
-        for (int i = 0; i < 128; ++i) mb = fmaxf(mb, x[i]);
+        for (int k = 0; k < 8; ++k) mxk[k] = fmaxf(x[k], x[k + 8]);
+#pragma unroll
+        for (int i = 16; i < 128; i += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mxk[k] = fmax3(mxk[k], x[i + k], x[i + 8 + k]);
+        const float mb = fmax3(fmax3(mxk[0], mxk[1], mxk[2]), fmax3(mxk[3], mxk[4], mxk[5]), fmaxf(mxk[6], mxk[7])) *
+                         mult;
         // ---- reference max: move it only when the block max exceeds it by more than 2^8
         float alpha = 1.f;
         bool rescale = false;
@@ -418,19 +451,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = mb;
         }
         const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-        // two row sums: of the bf16-rounded P the product uses (normalises O, so O is an exact convex
-        // combination of V rows) and of the unrounded P (for the LSE)
-        float rs = 0.f, rse = 0.f;
+        // ---- P = 2^(mult * x - m); two row sums: of the bf16-rounded P the product uses (normalises O:
+        // an exact convex combination of V rows) and of the unrounded P (for the LSE)
+        const uint64_t mul2 = f2_pack(mult, mult), neg2 = f2_pack(-mr, -mr);
+        uint64_t se[4] = {0, 0, 0, 0}, sr[4] = {0, 0, 0, 0};
         uint32_t pk[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          const float p0 = ex2_approx(x[2 * i] - mr), p1 = ex2_approx(x[2 * i + 1] - mr);
+          float y0, y1;
+          f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), mul2, neg2), y0, y1);
+          const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
           pk[i] = pack_bf16x2(p0, p1);
-          rs += bf16x2_sum(pk[i]);
-          rse += p0 + p1;
+          se[i & 3] = f2_add(se[i & 3], f2_pack(p0, p1));
+          sr[i & 3] = f2_add(sr[i & 3], f2_pack(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xFFFF0000u)));
         }
-        l = l * alpha + rs;
-        le = le * alpha + rse;
+        float e0, e1, r0, r1;
+        f2_unpack(f2_add(f2_add(se[0], se[1]), f2_add(se[2], se[3])), e0, e1);
+        f2_unpack(f2_add(f2_add(sr[0], sr[1]), f2_add(sr[2], sr[3])), r0, r1);
+        l = l * alpha + (r0 + r1);
+        le = le * alpha + (e0 + e1);
         // ---- the previous P V must be complete: P buffer free, O stable
         if (j > 0) {
           ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o[t], (uint32_t)((j - 1) & 1), wc));
@@ -450,10 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc5_wait_st();
         }
-        uint8_t* pbuf = sP[t];
 #pragma unroll
         for (int c16 = 0; c16 < 16; ++c16)
-          *reinterpret_cast<uint4*>(pbuf + tile_off(row, c16)) =
+          *reinterpret_cast<uint4*>(sPt + tile_off(row, c16)) =
               make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
         fence_proxy_async_smem();
         tc5_fence_before();
@@ -467,7 +505,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool empty = m_ref == -INFINITY;
         const float inv = empty ? 0.f : 1.f / l;
         // staging for the TMA store (both buffers are free: the last Q K^T and P V have completed)
-        uint8_t* st = sP[t];
         if (!a.out_f32) {
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -481,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               v.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
               v.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
               v.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
-              *reinterpret_cast<uint4*>(st + tile_off(row, c0 / 8 + q4)) = v;
+              *reinterpret_cast<uint4*>(sPt + tile_off(row, c0 / 8 + q4)) = v;
             }
           }
         } else {
@@ -491,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t o[32];
             tc5_ld32(tO + c0, o);
             tc5_wait_ld();
-            uint8_t* box = (c0 < 64 ? sP[t] : sQ[t]) + ((c0 >> 5) & 1) * 16384;
+            uint8_t* box = (c0 < 64 ? sPt : sQt) + ((c0 >> 5) & 1) * 16384;
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
               float4 v = make_float4(__uint_as_float(o[4 * q4 + 0]) * inv, __uint_as_float(o[4 * q4 + 1]) * inv,
@@ -506,20 +543,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // gave up (a failed wait always sets the CTA's abort flag)
       fence_proxy_async_smem();
       named_bar_sync(1 + t, 128);
-      if (!*wc.abort) {
-        uint8_t* st = sP[t];
-        if ((warp & 3) == 0 && lane == 0) {
-          if (!a.out_f32) {
+      if (!*wc.abort && (warp & 3) == 0 && lane == 0) {
+        if (!a.out_f32) {
 #pragma unroll
-            for (int x = 0; x < D / 64; ++x) tma_store_3d(&tmO, st + x * 16384, x * 64, r * 128, b * a.Hq + TT.h);
-          } else {
+          for (int x = 0; x < D / 64; ++x) tma_store_3d(&tmO, sPt + x * 16384, x * 64, r * 128, b * a.Hq + TT.h);
+        } else {
 #pragma unroll
-            for (int x = 0; x < D / 32; ++x)
-              tma_store_3d(&tmO, (x < 2 ? sP[t] : sQ[t]) + (x & 1) * 16384, x * 32, r * 128, b * a.Hq + TT.h);
-          }
-          bulk_commit_group();
-          bulk_wait_group_read0();
+          for (int x = 0; x < D / 32; ++x)
+            tma_store_3d(&tmO, (x < 2 ? sPt : sQt) + (x & 1) * 16384, x * 32, r * 128, b * a.Hq + TT.h);
         }
+        bulk_commit_group();
+        bulk_wait_group_read0();
       }
     }
   }
@@ -553,12 +587,11 @@ int launch_k(const FwdArgs& a, cudaStream_t st) {
   Tc5Params p;
   std::memset(&p, 0, sizeof(p));
   p.a = a;
-  const int HP = (a.Hq + 1) / 2;
-  p.n_pairs = a.B * a.mask.nq * HP;
+  const int n_pairs = a.B * a.mask.nq * ((a.Hq + 1) / 2);
   auto kern = fwd_tc5_kernel<D, SK>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
     return FA_ERR_CUDA;
-  kern<<<p.n_pairs, kThreads, C::kSmem, st>>>(p, tq, tk, tv, to);
+  kern<<<n_pairs, kThreads, C::kSmem, st>>>(p, tq, tk, tv, to);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
