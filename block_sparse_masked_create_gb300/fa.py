@@ -86,6 +86,11 @@ def load() -> ctypes.CDLL:
     lib.fa_flex_decode.restype = ctypes.c_int
     lib.fa_flex_decode.argtypes = [vp, vp, vp, vp, i32, P(BlockMaskC), P(ScoreRule), f32, vp, i32, vp, i32, i32, i32, i32,
                                    i32, i32, vp, sz, vp, vp, vp]
+    lib.fa_flex_decode_noalloc.restype = ctypes.c_int
+    lib.fa_flex_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, P(BlockMaskC), P(ScoreRule), f32, vp, i32, vp, i32,
+                                           i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.fa_decode_noalloc_scratch_bytes.restype = sz
+    lib.fa_decode_noalloc_scratch_bytes.argtypes = []
     lib.fa_block_mask_stats.restype = ctypes.c_int
     lib.fa_block_mask_stats.argtypes = [P(BlockMaskC), vp, vp]
     lib.fa_check_status.restype = ctypes.c_int
@@ -293,6 +298,27 @@ def flex_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, p
                                  d, page, max_pages, _ptr(workspace), workspace.numel(), _ptr(status),
                                  _ptr(counters), _stream(q.device)), "fa_flex_decode")
     return out, lse
+
+
+def decode_noalloc_scratch_bytes() -> int:
+    return int(load().fa_decode_noalloc_scratch_bytes())
+
+
+def flex_decode_noalloc(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, page_table: torch.Tensor,
+                        block_mask: BlockMask, score: Optional[ScoreRule] = None, scale: Optional[float] = None,
+                        out: torch.Tensor = None, lse: torch.Tensor = None, status: Optional[torch.Tensor] = None,
+                        counters: Optional[torch.Tensor] = None) -> int:
+    """fa_flex_decode_noalloc: the paged decode with its split workspace in the library's fixed device
+    array, for callers that cannot allocate. `out` and `lse` must be provided (nothing is allocated here).
+    Returns the fa_status code (FA_ERR_BUFFER_TOO_SMALL when the problem exceeds the fixed array)."""
+    if out is None or lse is None:
+        raise ValueError("out and lse must be provided")
+    Bz, Hq, d = q.shape
+    P, Hkv, page, _ = k_pages.shape
+    return int(load().fa_flex_decode_noalloc(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), P, ctypes.byref(block_mask.c),
+        ctypes.byref(score) if score else None, float(scale) if scale else 0.0, _ptr(out), _out_code(out), _ptr(lse),
+        Bz, Hq, Hkv, d, page, page_table.shape[1], _ptr(status), _ptr(counters), _stream(q.device)))
 
 
 def check_status(status: torch.Tensor) -> int:

@@ -205,6 +205,29 @@ FA_API fa_status fa_flex_decode(const void* q, const void* k_pages, const void* 
                                 int32_t max_pages, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                 int64_t* dev_counters, fa_stream_t stream);
 
+/* Allocation-free decode. The pages this library follows have no counterpart to this entry point; it
+ * exists for callers that cannot provide device memory: a host program whose device memory belongs to
+ * another runtime's pool, or a serving loop that must never call cudaMalloc / cudaFree (cudaFree
+ * synchronises the whole device). It computes exactly what fa_flex_decode computes (same arguments
+ * minus the workspace) and keeps the per-split state in one file-scope device array of
+ * FA_DECODE_NOALLOC_SCRATCH_BYTES bytes that every GPU loading libfa.so holds until the process exits.
+ *  - Set-up: the first call on a device, with that device current, looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *  - Size limit: a problem whose fa_decode_workspace_bytes(...) exceeds the array returns
+ *    FA_ERR_BUFFER_TOO_SMALL and launches nothing (fa_decode_noalloc_scratch_bytes() reports the size).
+ *  - Sharing: all calls use the same array. Calls that overlap on the GPU (different streams with no
+ *    ordering between them) race on it; calls on one stream are fine. Nothing in it needs clearing
+ *    between calls.
+ *  - It allocates no memory and calls no allocating routine. */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+FA_API fa_status fa_flex_decode_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                        const int32_t* page_table, int32_t n_pages_total,
+                                        const fa_block_mask* block_mask, const fa_score_rule* score_rule,
+                                        float scale, void* out, int32_t out_dtype, float* lse, int32_t Bz,
+                                        int32_t Hq, int32_t Hkv, int32_t d, int32_t page, int32_t max_pages,
+                                        int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream);
+FA_API size_t fa_decode_noalloc_scratch_bytes(void);
+
 /* Block statistics of a BlockMask ("5.1.2 FlexAttention ...", sections 2.2 and 6.3: full/partial/empty
  * counts and row lengths). dev_out: device int64[6] = {full, partial, empty, max row length (full +
  * partial), sum of row lengths, rows}. Enqueued on stream, no synchronisation. */
