@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(128) debug_tc5_gemm_kernel(const __nv_bfloat16
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(&tmem_base, 128);
+    tmem_alloc(&tmem_base, 256);  // D at columns [0, 128), A (mode 2) at [128, 128 + K/2)
     tmem_relinquish();
   }
   tc5_fence_before();
@@ -56,7 +56,18 @@ __global__ void __launch_bounds__(128) debug_tc5_gemm_kernel(const __nv_bfloat16
   WaitCtl wc{timeout_ns, status, &s_abort};
   const uint32_t tmem = tmem_base;
   bool ok = true;
-  if (use_tma) {
+  if (use_tma == 2) {
+    // A into tensor memory: thread = row, K packed two bf16 per 32-bit column
+    const int row = warp * 32 + lane;
+    for (int c0 = 0; c0 < K / 2; c0 += 32) {
+      uint32_t r[32];
+      for (int j = 0; j < 32; ++j)
+        r[j] = *reinterpret_cast<const uint32_t*>(A + (size_t)row * K + 2 * (c0 + j));
+      tc5_st32(tmem + ((uint32_t)(warp * 32) << 16) + 128u + (uint32_t)c0, r);
+    }
+    tc5_wait_st();
+  }
+  if (use_tma == 1) {
     if (tid == 0) {
       const uint32_t bytes = 2u * 128u * (uint32_t)K * 2u;
       mbar_arrive_expect_tx(&bar_load, bytes);
@@ -69,7 +80,7 @@ __global__ void __launch_bounds__(128) debug_tc5_gemm_kernel(const __nv_bfloat16
     }
     ok = mbar_wait(&bar_load, 0, wc);
   } else {
-    for (int x = tid; x < 128 * K / 8; x += 128) {  // A: 16-byte chunks
+    for (int x = tid; use_tma == 0 && x < 128 * K / 8; x += 128) {  // A: 16-byte chunks
       const int row = x / (K / 8), ch = x % (K / 8);
       const uint4 val = *reinterpret_cast<const uint4*>(A + (size_t)row * K + ch * 8);
       *reinterpret_cast<uint4*>(sA + (ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) = val;
@@ -89,6 +100,7 @@ __global__ void __launch_bounds__(128) debug_tc5_gemm_kernel(const __nv_bfloat16
     }
     fence_proxy_async_smem();
   }
+  tc5_fence_before();  // orders the tensor-memory stores of mode 2 before the MMA issue
   __syncthreads();
   tc5_fence_after();
   if (ok && tid == 0) {
@@ -98,7 +110,10 @@ __global__ void __launch_bounds__(128) debug_tc5_gemm_kernel(const __nv_bfloat16
       const uint64_t ad = sdesc_sw128(a0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
       const uint64_t bd = b_mn ? sdesc_sw128(b0 + ks * 16 * 128, K * 128, 1024)
                                : sdesc_sw128(b0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-      tc5_mma_ss(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+      if (use_tma == 2)
+        tc5_mma_ts(tmem, tmem + 128u + (uint32_t)(ks * 8), bd, idesc, ks > 0 ? 1u : 0u);
+      else
+        tc5_mma_ss(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
     }
     tc5_commit(&bar_mma);
   }
@@ -116,12 +131,12 @@ __global__ void __launch_bounds__(128) debug_tc5_gemm_kernel(const __nv_bfloat16
     }
   }
   if (!ok && tid == 0) {  // nothing may still be writing shared or tensor memory when the CTA leaves
-    if (use_tma) mbar_wait_drain(&bar_load, 0, timeout_ns);
+    if (use_tma == 1) mbar_wait_drain(&bar_load, 0, timeout_ns);
     mbar_wait_drain(&bar_mma, 0, timeout_ns);
   }
   tc5_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 128);
+  if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 }  // namespace

@@ -9,18 +9,19 @@
 //
 // How (one CTA = two 128-row query tiles of sibling heads of the same query block, 10 warps):
 //   warps 0-3 / 4-7  softmax warpgroups of tile 0 / tile 1 (TMEM lane = query row = thread). Per block:
-//                    S from TMEM to registers, "S free" signal, score rule, mask, row max (3-input max
-//                    tree), P = 2^(x - m) with packed fp32x2 FMAs, row sums, P as bf16 into shared
-//                    memory (128-byte swizzled K-major layout), "P ready" signal. The O accumulator is
-//                    rescaled in TMEM only when the running max grows by more than 2^8 (exact for any
-//                    reference max; the bound keeps P <= 256). Epilogue O / l -> TMA store.
+//                    S from TMEM to registers, score rule, mask, row max (3-input max tree),
+//                    P = 2^(x - m) with packed fp32x2 FMAs, two row sums, P as bf16 back into tensor
+//                    memory over the S columns it came from, "P ready". The O accumulator is rescaled in
+//                    TMEM only when the running max grows by more than 2^8 (exact for any reference max;
+//                    the bound keeps P <= 256). Epilogue O / l -> shared memory -> TMA store.
 //   warp 8           TMA producer: Q tiles, then K / V tiles of the visited blocks only (an empty block
-//                    issues no load) into a ring of shared-memory slots, in exactly the order the MMA
-//                    warp consumes them. Sibling query heads of one KV head with the same mask row share
-//                    each K / V load.
-//   warp 9           allocates TMEM (S and O of both tiles: 512 columns) and issues every tcgen05.mma from
-//                    one thread. S_t(j+1) = Q_t K(j+1)^T is issued as soon as the softmax has read S_t(j)
-//                    (so it overlaps the softmax of block j), O_t += P_t(j) V(j) when P_t(j) is ready.
+//                    issues no load) into a 5-slot ring, in exactly the order the MMA warp consumes them.
+//                    Sibling query heads of one KV head with the same mask row share each K / V load.
+//   warp 9           allocates TMEM (S/P and O of both tiles: 512 columns) and issues every tcgen05.mma
+//                    from one thread: when P_t(j) is ready, O_t += P_t(j) V(j) (A read from TMEM) and then
+//                    S_t(j+1) = Q_t K(j+1)^T (A, B from shared memory). The tensor pipe runs a thread's MMAs
+//                    in issue order, so S_t(j+1) overwrites P_t(j) only after the product has read it, and
+//                    the completion of S_t(j) implies that of O_t's previous update.
 // Two tiles in flight keep the tensor core busy while each warpgroup runs its softmax. Every wait is
 // bounded (an abort flag stops all roles; copies and MMAs in flight are drained before tensor memory is
 // freed and the CTA exits).
@@ -42,15 +43,14 @@ enum ScoreKind { SK_NONE = 0, SK_ALIBI = 1, SK_SOFTCAP = 2, SK_GENERIC = 3 };
 
 template <int D>
 struct Tc5Cfg {
-  static constexpr int kQBytes = 128 * D * 2;      // one Q tile
-  static constexpr int kPBytes = 128 * 128 * 2;    // one P tile (also the O staging tile)
+  static constexpr int kQBytes = 128 * D * 2;      // one Q tile (also the O staging tile)
   static constexpr int kSlotBytes = 128 * D * 2;   // one K or V tile
-  static constexpr int kStages = D == 128 ? 3 : 6;
-  static constexpr int kOffP = 2 * kQBytes;
-  static constexpr int kOffRing = kOffP + 2 * kPBytes;
+  static constexpr int kStages = D == 128 ? 5 : 12;
+  static constexpr int kOffRing = 2 * kQBytes;
   static constexpr int kSmem = kOffRing + kStages * kSlotBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  // tensor-memory columns: S of tile t at [256 t, 256 t + 128), O of tile t at [256 t + 128, 256 t + 128 + D)
+  // tensor-memory columns: S_t (and P_t over its first 64 columns) at [256 t, 256 t + 128),
+  // O_t at [256 t + 128, 256 t + 128 + D)
   __device__ static constexpr uint32_t col_s(int t) { return (uint32_t)t * 256u; }
   __device__ static constexpr uint32_t col_o(int t) { return (uint32_t)t * 256u + 128u; }
 };
@@ -101,8 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const FwdArgs& a = P.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q[2], bar_s[2], bar_sfree[2], bar_p[2], bar_o[2], bar_full[NST], bar_empty[NST],
-      bar_drain;
+  __shared__ uint64_t bar_q[2], bar_s[2], bar_p[2], bar_o[2], bar_full[NST], bar_empty[NST], bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int32_t s_abort;
 
@@ -124,8 +123,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* sQ0 = smem;
   uint8_t* sQ1 = smem + C::kQBytes;
-  uint8_t* sP0 = smem + C::kOffP;
-  uint8_t* sP1 = smem + C::kOffP + C::kPBytes;
   uint8_t* sRing = smem + C::kOffRing;
 
   if (tid == 0) {
@@ -134,7 +131,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_q[t], 1);
       mbar_init(&bar_s[t], 1);
-      mbar_init(&bar_sfree[t], 128);
       mbar_init(&bar_p[t], 128);
       mbar_init(&bar_o[t], 1);
     }
@@ -164,8 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kLoadWarp) {
     // =============================== TMA producer ===============================
     // load order == consumption order of the MMA warp:
-    //   separate K/V: K0(0) K1(0), then per j: K0(j+1) K1(j+1) V0(j) V1(j)   (each only if it exists)
-    //   shared K/V:   K(0), then per j: K(j+1) V(j)
+    //   separate K/V: K0(0) K1(0), then per j: V0(j) K0(j+1) V1(j) K1(j+1)   (each only if it exists)
+    //   shared K/V:   K(0), then per j: V(j) K(j+1)
     if (lane == 0) {
       if (a.counters) {
         unsigned long long* cnt = reinterpret_cast<unsigned long long*>(a.counters);
@@ -202,17 +198,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (shared_kv) {
         ok = load(T0, false, 0);
         for (int j = 0; j < T0.n && ok; ++j) {
-          if (j + 1 < T0.n) ok = load(T0, false, j + 1);
-          if (ok) ok = load(T0, true, j);
+          ok = load(T0, true, j);
+          if (ok && j + 1 < T0.n) ok = load(T0, false, j + 1);
         }
       } else {
         if (T0.n > 0) ok = load(T0, false, 0);
         if (ok && T1.n > 0) ok = load(T1, false, 0);
         for (int j = 0; j < nmax && ok; ++j) {
-          if (j + 1 < T0.n) ok = load(T0, false, j + 1);
-          if (ok && j + 1 < T1.n) ok = load(T1, false, j + 1);
-          if (ok && j < T0.n) ok = load(T0, true, j);
-          if (ok && j < T1.n) ok = load(T1, true, j);
+          if (j < T0.n) {
+            ok = load(T0, true, j);
+            if (ok && j + 1 < T0.n) ok = load(T0, false, j + 1);
+          }
+          if (ok && j < T1.n) {
+            ok = load(T1, true, j);
+            if (ok && j + 1 < T1.n) ok = load(T1, false, j + 1);
+          }
         }
       }
       if (!ok || *wc.abort) {
@@ -251,22 +251,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc5_commit(&bar_s[t]);
       };
       auto mma_pv = [&](int t, int s, bool acc) {
-        const uint32_t pa = smem_u32(t ? sP1 : sP0), va = smem_u32(sRing + s * C::kSlotBytes);
+        const uint32_t va = smem_u32(sRing + s * C::kSlotBytes);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t offp = (ks >> 2) * 16384 + (ks & 3) * 32;
-          tc5_mma_ss(tmem + C::col_o(t), sdesc_sw128(pa + offp, 16, 1024),
+        for (int ks = 0; ks < 8; ++ks)
+          tc5_mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + (uint32_t)(ks * 8),
                      sdesc_sw128(va + ks * 2048, 128 * 128, 1024), idesc_pv, (acc || ks > 0) ? 1u : 0u);
-        }
         tc5_commit(&bar_o[t]);
       };
       auto wait_p = [&](int t, int j) -> bool {
         if (!mbar_wait(&bar_p[t], (uint32_t)(j & 1), wc)) return false;
-        tc5_fence_after();
-        return true;
-      };
-      auto wait_sfree = [&](int t, int j) -> bool {
-        if (!mbar_wait(&bar_sfree[t], (uint32_t)(j & 1), wc)) return false;
         tc5_fence_after();
         return true;
       };
@@ -281,21 +274,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc5_commit(&bar_empty[sk]);
           }
           for (int j = 0; j < n && ok; ++j) {
-            if (j + 1 < n) {
-              if (!(ok = wait_sfree(0, j))) break;
-              if ((sk = take()) < 0) { ok = false; break; }
-              mma_qk(0, sk);
-              if (!(ok = wait_sfree(1, j))) break;
-              mma_qk(1, sk);
-              tc5_commit(&bar_empty[sk]);
-            }
             if (!(ok = wait_p(0, j))) break;
             const int sv = take();
             if (sv < 0) { ok = false; break; }
             mma_pv(0, sv, j > 0);
+            sk = -1;
+            if (j + 1 < n) {
+              if ((sk = take()) < 0) { ok = false; break; }
+              mma_qk(0, sk);
+            }
             if (!(ok = wait_p(1, j))) break;
             mma_pv(1, sv, j > 0);
             tc5_commit(&bar_empty[sv]);
+            if (sk >= 0) {
+              mma_qk(1, sk);
+              tc5_commit(&bar_empty[sk]);
+            }
           }
         } else {
           const Tile* TT[2] = {&T0, &T1};
@@ -310,21 +304,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < nmax && ok; ++j) {
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-              if (!ok || j + 1 >= TT[t]->n) continue;
-              if (!(ok = wait_sfree(t, j))) break;
-              const int s = take();
-              if (s < 0) { ok = false; break; }
-              mma_qk(t, s);
-              tc5_commit(&bar_empty[s]);
-            }
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
               if (!ok || j >= TT[t]->n) continue;
               if (!(ok = wait_p(t, j))) break;
-              const int s = take();
-              if (s < 0) { ok = false; break; }
-              mma_pv(t, s, j > 0);
-              tc5_commit(&bar_empty[s]);
+              const int sv = take();
+              if (sv < 0) { ok = false; break; }
+              mma_pv(t, sv, j > 0);
+              tc5_commit(&bar_empty[sv]);
+              if (j + 1 < TT[t]->n) {
+                const int sk = take();
+                if (sk < 0) { ok = false; break; }
+                mma_qk(t, sk);
+                tc5_commit(&bar_empty[sk]);
+              }
             }
           }
         }
@@ -339,7 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = (warp & 3) * 32 + lane;  // TMEM lane == query row in the tile
     const Tile TT = t ? T1 : T0;
     uint8_t* const sQt = t ? sQ1 : sQ0;
-    uint8_t* const sPt = t ? sP1 : sP0;
     const int q_row = r * 128 + row;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::col_s(t);
@@ -376,9 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 32) tc5_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&x[c0]));
         tc5_wait_ld();
-        // S is in registers: the MMA warp may overwrite it with the next block's scores
-        tc5_fence_before();
-        mbar_arrive(&bar_sfree[t]);
         const bool partial = j >= TT.n_full;
         const bool need_col = partial || SK != SK_NONE;
         const int c = need_col ? TT.col(j) : 0;
@@ -470,12 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         f2_unpack(f2_add(f2_add(sr[0], sr[1]), f2_add(sr[2], sr[3])), r0, r1);
         l = l * alpha + (r0 + r1);
         le = le * alpha + (e0 + e1);
-        // ---- the previous P V must be complete: P buffer free, O stable
-        if (j > 0) {
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o[t], (uint32_t)((j - 1) & 1), wc));
-          if (!ok) break;
-          tc5_fence_after();
-        }
+        // ---- O is stable here: S_t(j) completed, and O_t's previous update was issued before it
         if (__any_sync(0xFFFFFFFFu, rescale)) {
           const float f = rescale ? alpha : 1.f;
 #pragma unroll
@@ -487,13 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
             tc5_st32(tO + c0, o);
           }
-          tc5_wait_st();
         }
-#pragma unroll
-        for (int c16 = 0; c16 < 16; ++c16)
-          *reinterpret_cast<uint4*>(sPt + tile_off(row, c16)) =
-              make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-        fence_proxy_async_smem();
+        // ---- P into tensor memory over S's first 64 columns (two bf16 per column)
+        tc5_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tc5_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        tc5_wait_st();
         tc5_fence_before();
         mbar_arrive(&bar_p[t]);
       }
@@ -501,59 +481,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o[t], (uint32_t)((TT.n - 1) & 1), wc));
       tc5_fence_after();
-      if (ok) {
-        const bool empty = m_ref == -INFINITY;
-        const float inv = empty ? 0.f : 1.f / l;
-        // staging for the TMA store (both buffers are free: the last Q K^T and P V have completed)
-        if (!a.out_f32) {
+      const bool empty = m_ref == -INFINITY;
+      const float inv = empty ? 0.f : 1.f / l;
+      if (ok && q_row < a.q_len) Lg[q_row] = empty ? -INFINITY : (m_ref + __log2f(le)) * kLn2;
+      // staging in this tile's Q buffer (free: every Q K^T of the tile has completed). bf16: one pass of
+      // D/64 boxes [128][64]; fp32: one pass per 32 columns, each one box [128][32] (128-byte rows).
+      const int passes = a.out_f32 ? D / 32 : 1;
+      for (int ps = 0; ps < passes; ++ps) {
+        if (ok) {
+          if (!a.out_f32) {
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tc5_ld32(tO + c0, o);
-            tc5_wait_ld();
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tc5_ld32(tO + c0, o);
+              tc5_wait_ld();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
-              *reinterpret_cast<uint4*>(sPt + tile_off(row, c0 / 8 + q4)) = v;
+              for (int q4 = 0; q4 < 4; ++q4) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
+                v.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
+                v.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
+                v.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
+                *reinterpret_cast<uint4*>(sQt + tile_off(row, c0 / 8 + q4)) = v;
+              }
             }
-          }
-        } else {
-          // fp32: D/32 boxes of [128][32] floats (128-byte rows); boxes 0-1 in the P buffer, 2-3 in Q's
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          } else {
             uint32_t o[32];
-            tc5_ld32(tO + c0, o);
+            tc5_ld32(tO + ps * 32, o);
             tc5_wait_ld();
-            uint8_t* box = (c0 < 64 ? sPt : sQt) + ((c0 >> 5) & 1) * 16384;
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
               float4 v = make_float4(__uint_as_float(o[4 * q4 + 0]) * inv, __uint_as_float(o[4 * q4 + 1]) * inv,
                                      __uint_as_float(o[4 * q4 + 2]) * inv, __uint_as_float(o[4 * q4 + 3]) * inv);
-              *reinterpret_cast<float4*>(box + row * 128 + ((q4 ^ (row & 7)) << 4)) = v;
+              *reinterpret_cast<float4*>(sQt + row * 128 + ((q4 ^ (row & 7)) << 4)) = v;
             }
           }
         }
-        if (q_row < a.q_len) Lg[q_row] = empty ? -INFINITY : (m_ref + __log2f(le)) * kLn2;
-      }
-      // every thread of the warpgroup reaches this barrier (ok or not); the store runs only if no role
-      // gave up (a failed wait always sets the CTA's abort flag)
-      fence_proxy_async_smem();
-      named_bar_sync(1 + t, 128);
-      if (!*wc.abort && (warp & 3) == 0 && lane == 0) {
-        if (!a.out_f32) {
+        // every thread of the warpgroup reaches these barriers (ok or not); the store runs only if no
+        // role gave up (a failed wait always sets the CTA's abort flag)
+        fence_proxy_async_smem();
+        named_bar_sync(1 + t, 128);
+        if (!*wc.abort && (warp & 3) == 0 && lane == 0) {
+          if (!a.out_f32) {
 #pragma unroll
-          for (int x = 0; x < D / 64; ++x) tma_store_3d(&tmO, sPt + x * 16384, x * 64, r * 128, b * a.Hq + TT.h);
-        } else {
-#pragma unroll
-          for (int x = 0; x < D / 32; ++x)
-            tma_store_3d(&tmO, (x < 2 ? sPt : sQt) + (x & 1) * 16384, x * 32, r * 128, b * a.Hq + TT.h);
+            for (int x = 0; x < D / 64; ++x) tma_store_3d(&tmO, sQt + x * 16384, x * 64, r * 128, b * a.Hq + TT.h);
+          } else {
+            tma_store_3d(&tmO, sQt, ps * 32, r * 128, b * a.Hq + TT.h);
+          }
+          bulk_commit_group();
+          bulk_wait_group_read0();
         }
-        bulk_commit_group();
-        bulk_wait_group_read0();
+        named_bar_sync(1 + t, 128);  // the staging buffer is free again
       }
     }
   }

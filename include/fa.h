@@ -250,7 +250,8 @@ FA_API fa_status fa_debug_wait_timeout(int32_t* dev_status, uint64_t timeout_ns,
  * C = A * B^T with A device bf16 [128, K] and B device bf16 [128, K] (b_mn_major = 0, B K-major), or
  * C = A * B with B device bf16 [K, 128] (b_mn_major = 1, B MN-major); C device fp32 [128, 128].
  * K in {64, 128}. use_tma = 1 stages the tiles with TMA (128-byte swizzle), 0 with plain stores in the
- * same swizzled layout. Used by the tests to pin the shared-memory and instruction descriptors. */
+ * same swizzled layout, 2 puts A in tensor memory (row per lane, two bf16 per 32-bit column) and B in
+ * shared memory. Used by the tests to pin the shared-memory, tensor-memory and instruction descriptors. */
 FA_API fa_status fa_debug_tc5_gemm(const void* A, const void* B, float* C, int32_t K, int32_t b_mn_major,
                             int32_t use_tma, int32_t* dev_status, fa_stream_t stream);
 

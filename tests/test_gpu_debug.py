@@ -19,7 +19,7 @@ def test_bounded_wait_reports_timeout():
 
 @pytest.mark.parametrize("K", [64, 128])
 @pytest.mark.parametrize("b_mn", [False, True])
-@pytest.mark.parametrize("use_tma", [False, True])
+@pytest.mark.parametrize("use_tma", [0, 1, 2], ids=["st", "tma", "a_tmem"])
 def test_tc5_gemm_descriptors(K, b_mn, use_tma):
     g = torch.Generator(device="cpu").manual_seed(K * 4 + 2 * b_mn + use_tma)
     A = torch.randn(128, K, generator=g).to(torch.bfloat16).cuda()
