@@ -445,9 +445,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          float y0, y1;
-          f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), mul2, neg2), y0, y1);
-          const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+          const uint64_t y2 = f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), mul2, neg2);
+          float p0, p1;
+          if ((i & 3) == 3) {  // a quarter of the exponentials on the FMA pipe, the rest on MUFU
+            f2_unpack(f2_exp2_poly(y2), p0, p1);
+          } else {
+            float y0, y1;
+            f2_unpack(y2, y0, y1);
+            p0 = ex2_approx(y0);
+            p1 = ex2_approx(y1);
+          }
           pk[i] = pack_bf16x2(p0, p1);
           se[i & 3] = f2_add(se[i & 3], f2_pack(p0, p1));
           sr[i & 3] = f2_add(sr[i & 3], f2_pack(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xFFFF0000u)));

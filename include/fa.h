@@ -255,6 +255,11 @@ FA_API fa_status fa_debug_wait_timeout(int32_t* dev_status, uint64_t timeout_ns,
 FA_API fa_status fa_debug_tc5_gemm(const void* A, const void* B, float* C, int32_t K, int32_t b_mn_major,
                             int32_t use_tma, int32_t* dev_status, fa_stream_t stream);
 
+/* Self-test of the two exponentials the forward kernel mixes: y_poly[i] = 2^x[i] from the FMA-pipe
+ * polynomial (range reduction + cubic, max relative error 7.5e-5), y_mufu[i] = 2^x[i] from ex2.approx.
+ * x, y_poly, y_mufu: device fp32 [n]. */
+FA_API fa_status fa_debug_exp2(const float* x, float* y_poly, float* y_mufu, int32_t n, fa_stream_t stream);
+
 /* Library version string. */
 FA_API const char* fa_version(void);
 
