@@ -159,171 +159,178 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kLoadWarp) {
     // =============================== TMA producer ===============================
-    // load order == consumption order of the MMA warp:
+    // The whole warp runs this code (operands stay warp-uniform); elect.sync picks the lane that issues.
+    // Load order == consumption order of the MMA warp:
     //   separate K/V: K0(0) K1(0), then per j: V0(j) K0(j+1) V1(j) K1(j+1)   (each only if it exists)
     //   shared K/V:   K(0), then per j: V(j) K(j+1)
-    if (lane == 0) {
-      if (a.counters) {
-        unsigned long long* cnt = reinterpret_cast<unsigned long long*>(a.counters);
-        const int vis = T0.n + T1.n;
-        atomicAdd(cnt + 0, (unsigned long long)(T0.valid + T1.valid));
-        atomicAdd(cnt + 1, (unsigned long long)(T0.n_full + T1.n_full));
-        atomicAdd(cnt + 2, (unsigned long long)(T0.n - T0.n_full + T1.n - T1.n_full));
-        atomicAdd(cnt + 3, (unsigned long long)(shared_kv ? vis : 2 * vis));
-      }
-      if (T0.n > 0) {
-        mbar_arrive_expect_tx(&bar_q[0], C::kQBytes);
+    if (a.counters && lane == 0) {
+      unsigned long long* cnt = reinterpret_cast<unsigned long long*>(a.counters);
+      const int vis = T0.n + T1.n;
+      atomicAdd(cnt + 0, (unsigned long long)(T0.valid + T1.valid));
+      atomicAdd(cnt + 1, (unsigned long long)(T0.n_full + T1.n_full));
+      atomicAdd(cnt + 2, (unsigned long long)(T0.n - T0.n_full + T1.n - T1.n_full));
+      atomicAdd(cnt + 3, (unsigned long long)(shared_kv ? vis : 2 * vis));
+    }
+    __syncwarp();
+    if (T0.n > 0) {
+      mbar_arrive_expect_tx_elect(&bar_q[0], C::kQBytes);
 #pragma unroll
-        for (int x = 0; x < D / 64; ++x) tma_load_3d(sQ0 + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T0.h, &bar_q[0]);
-      }
-      if (T1.n > 0) {
-        mbar_arrive_expect_tx(&bar_q[1], C::kQBytes);
+      for (int x = 0; x < D / 64; ++x) tma_load_3d_elect(sQ0 + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T0.h, &bar_q[0]);
+    }
+    if (T1.n > 0) {
+      mbar_arrive_expect_tx_elect(&bar_q[1], C::kQBytes);
 #pragma unroll
-        for (int x = 0; x < D / 64; ++x) tma_load_3d(sQ1 + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T1.h, &bar_q[1]);
-      }
-      int issued = 0;
-      bool ok = true;
-      auto load = [&](const Tile& T, bool is_v, int j) -> bool {
-        const int s = issued % NST;
-        if (issued >= NST && !mbar_wait(&bar_empty[s], (uint32_t)(((issued / NST) - 1) & 1), wc)) return false;
-        const int c = T.col(j);
-        uint8_t* dst = sRing + s * C::kSlotBytes;
-        mbar_arrive_expect_tx(&bar_full[s], C::kSlotBytes);
+      for (int x = 0; x < D / 64; ++x) tma_load_3d_elect(sQ1 + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T1.h, &bar_q[1]);
+    }
+    int issued = 0;
+    bool ok = true;
+    auto load = [&](const Tile& T, bool is_v, int j) -> bool {
+      const int s = issued % NST;
+      if (issued >= NST &&
+          !__all_sync(0xFFFFFFFFu, mbar_wait(&bar_empty[s], (uint32_t)(((issued / NST) - 1) & 1), wc)))
+        return false;
+      const int c = T.col(j);
+      uint8_t* dst = sRing + s * C::kSlotBytes;
+      mbar_arrive_expect_tx_elect(&bar_full[s], C::kSlotBytes);
 #pragma unroll
-        for (int x = 0; x < D / 64; ++x)
-          tma_load_3d(dst + x * 16384, is_v ? &tmV : &tmK, x * 64, c * 128, b * a.Hkv + T.hk, &bar_full[s]);
-        ++issued;
-        return true;
-      };
-      if (shared_kv) {
-        ok = load(T0, false, 0);
-        for (int j = 0; j < T0.n && ok; ++j) {
+      for (int x = 0; x < D / 64; ++x)
+        tma_load_3d_elect(dst + x * 16384, is_v ? &tmV : &tmK, x * 64, c * 128, b * a.Hkv + T.hk, &bar_full[s]);
+      ++issued;
+      return true;
+    };
+    if (shared_kv) {
+      ok = load(T0, false, 0);
+      for (int j = 0; j < T0.n && ok; ++j) {
+        ok = load(T0, true, j);
+        if (ok && j + 1 < T0.n) ok = load(T0, false, j + 1);
+      }
+    } else {
+      if (T0.n > 0) ok = load(T0, false, 0);
+      if (ok && T1.n > 0) ok = load(T1, false, 0);
+      for (int j = 0; j < nmax && ok; ++j) {
+        if (j < T0.n) {
           ok = load(T0, true, j);
           if (ok && j + 1 < T0.n) ok = load(T0, false, j + 1);
         }
-      } else {
-        if (T0.n > 0) ok = load(T0, false, 0);
-        if (ok && T1.n > 0) ok = load(T1, false, 0);
-        for (int j = 0; j < nmax && ok; ++j) {
-          if (j < T0.n) {
-            ok = load(T0, true, j);
-            if (ok && j + 1 < T0.n) ok = load(T0, false, j + 1);
-          }
-          if (ok && j < T1.n) {
-            ok = load(T1, true, j);
-            if (ok && j + 1 < T1.n) ok = load(T1, false, j + 1);
-          }
+        if (ok && j < T1.n) {
+          ok = load(T1, true, j);
+          if (ok && j + 1 < T1.n) ok = load(T1, false, j + 1);
         }
       }
-      if (!ok || *wc.abort) {
-        // drain: the last NST issued copies may still be landing in shared memory
-        for (int i = max(0, issued - NST); i < issued; ++i)
-          mbar_wait_drain(&bar_full[i % NST], (uint32_t)((i / NST) & 1), a.timeout_ns);
-        if (T0.n > 0) mbar_wait_drain(&bar_q[0], 0, a.timeout_ns);
-        if (T1.n > 0) mbar_wait_drain(&bar_q[1], 0, a.timeout_ns);
-      }
+    }
+    if (!ok || *wc.abort) {
+      // drain: the last NST issued copies may still be landing in shared memory
+      for (int i = max(0, issued - NST); i < issued; ++i)
+        mbar_wait_drain(&bar_full[i % NST], (uint32_t)((i / NST) & 1), a.timeout_ns);
+      if (T0.n > 0) mbar_wait_drain(&bar_q[0], 0, a.timeout_ns);
+      if (T1.n > 0) mbar_wait_drain(&bar_q[1], 0, a.timeout_ns);
     }
   } else if (warp == kMmaWarp) {
     // =============================== MMA issuer ===============================
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-      int consumed = 0;
-      bool ok = true;
-      if (T0.n > 0) ok = mbar_wait(&bar_q[0], 0, wc);
-      if (ok && T1.n > 0) ok = mbar_wait(&bar_q[1], 0, wc);
+    // Warp-uniform like the producer; each tcgen05.mma / commit is issued by one elected lane.
+    // Descriptors: base values computed once, per-MMA offsets added to the 14-bit address field.
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+    const uint64_t qdesc0 = sdesc_sw128(smem_u32(sQ0), 16, 1024), qdesc1 = sdesc_sw128(smem_u32(sQ1), 16, 1024);
+    const uint64_t kdesc = sdesc_sw128(smem_u32(sRing), 16, 1024);
+    const uint64_t vdesc = sdesc_sw128(smem_u32(sRing), 128 * 128, 1024);
+    int consumed = 0;
+    bool ok = true;
+    if (T0.n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_q[0], 0, wc));
+    if (ok && T1.n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_q[1], 0, wc));
+    tc5_fence_after();
+    auto take = [&]() -> int {  // wait for the next ring slot in load order
+      const int s = consumed % NST;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_full[s], (uint32_t)((consumed / NST) & 1), wc))) return -1;
       tc5_fence_after();
-      auto take = [&]() -> int {  // wait for the next ring slot in load order
-        const int s = consumed % NST;
-        if (!mbar_wait(&bar_full[s], (uint32_t)((consumed / NST) & 1), wc)) return -1;
-        tc5_fence_after();
-        ++consumed;
-        return s;
-      };
-      auto mma_qk = [&](int t, int s) {
-        const uint32_t qa = smem_u32(t ? sQ1 : sQ0), ka = smem_u32(sRing + s * C::kSlotBytes);
+      ++consumed;
+      return s;
+    };
+    auto mma_qk = [&](int t, int s) {
+      const uint64_t qd = t ? qdesc1 : qdesc0;
+      const uint64_t kd = kdesc + (uint64_t)(s * (C::kSlotBytes >> 4));
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          tc5_mma_ss(tmem + C::col_s(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                     idesc_qk, ks > 0 ? 1u : 0u);
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+        tc5_mma_ss_elect(tmem + C::col_s(t), qd + off, kd + off, idesc_qk, ks > 0 ? 1u : 0u);
+      }
+      tc5_commit_elect(&bar_s[t]);
+    };
+    auto mma_pv = [&](int t, int s, bool acc) {
+      const uint64_t vd = vdesc + (uint64_t)(s * (C::kSlotBytes >> 4));
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        tc5_mma_ts_elect(tmem + C::col_o(t), tmem + C::col_s(t) + (uint32_t)(ks * 8), vd + (uint64_t)((ks * 2048) >> 4),
+                         idesc_pv, (acc || ks > 0) ? 1u : 0u);
+      tc5_commit_elect(&bar_o[t]);
+    };
+    auto wait_p = [&](int t, int j) -> bool {
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar_p[t], (uint32_t)(j & 1), wc))) return false;
+      tc5_fence_after();
+      return true;
+    };
+    if (ok) {
+      if (shared_kv) {
+        const int n = T0.n;
+        int sk = take();
+        ok = sk >= 0;
+        if (ok) {
+          mma_qk(0, sk);
+          mma_qk(1, sk);
+          tc5_commit_elect(&bar_empty[sk]);
         }
-        tc5_commit(&bar_s[t]);
-      };
-      auto mma_pv = [&](int t, int s, bool acc) {
-        const uint32_t va = smem_u32(sRing + s * C::kSlotBytes);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc5_mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + (uint32_t)(ks * 8),
-                     sdesc_sw128(va + ks * 2048, 128 * 128, 1024), idesc_pv, (acc || ks > 0) ? 1u : 0u);
-        tc5_commit(&bar_o[t]);
-      };
-      auto wait_p = [&](int t, int j) -> bool {
-        if (!mbar_wait(&bar_p[t], (uint32_t)(j & 1), wc)) return false;
-        tc5_fence_after();
-        return true;
-      };
-      if (ok) {
-        if (shared_kv) {
-          const int n = T0.n;
-          int sk = take();
-          ok = sk >= 0;
-          if (ok) {
+        for (int j = 0; j < n && ok; ++j) {
+          if (!(ok = wait_p(0, j))) break;
+          const int sv = take();
+          if (sv < 0) { ok = false; break; }
+          mma_pv(0, sv, j > 0);
+          sk = -1;
+          if (j + 1 < n) {
+            if ((sk = take()) < 0) { ok = false; break; }
             mma_qk(0, sk);
+          }
+          if (!(ok = wait_p(1, j))) break;
+          mma_pv(1, sv, j > 0);
+          tc5_commit_elect(&bar_empty[sv]);
+          if (sk >= 0) {
             mma_qk(1, sk);
-            tc5_commit(&bar_empty[sk]);
+            tc5_commit_elect(&bar_empty[sk]);
           }
-          for (int j = 0; j < n && ok; ++j) {
-            if (!(ok = wait_p(0, j))) break;
-            const int sv = take();
-            if (sv < 0) { ok = false; break; }
-            mma_pv(0, sv, j > 0);
-            sk = -1;
-            if (j + 1 < n) {
-              if ((sk = take()) < 0) { ok = false; break; }
-              mma_qk(0, sk);
-            }
-            if (!(ok = wait_p(1, j))) break;
-            mma_pv(1, sv, j > 0);
-            tc5_commit(&bar_empty[sv]);
-            if (sk >= 0) {
-              mma_qk(1, sk);
-              tc5_commit(&bar_empty[sk]);
-            }
-          }
-        } else {
-          const Tile* TT[2] = {&T0, &T1};
+        }
+      } else {
+        if (T0.n > 0) {
+          const int s = take();
+          if (s < 0) ok = false;
+          else { mma_qk(0, s); tc5_commit_elect(&bar_empty[s]); }
+        }
+        if (ok && T1.n > 0) {
+          const int s = take();
+          if (s < 0) ok = false;
+          else { mma_qk(1, s); tc5_commit_elect(&bar_empty[s]); }
+        }
+        for (int j = 0; j < nmax && ok; ++j) {
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (!ok || TT[t]->n == 0) continue;
-            const int s = take();
-            if (s < 0) { ok = false; break; }
-            mma_qk(t, s);
-            tc5_commit(&bar_empty[s]);
-          }
-          for (int j = 0; j < nmax && ok; ++j) {
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              if (!ok || j >= TT[t]->n) continue;
-              if (!(ok = wait_p(t, j))) break;
-              const int sv = take();
-              if (sv < 0) { ok = false; break; }
-              mma_pv(t, sv, j > 0);
-              tc5_commit(&bar_empty[sv]);
-              if (j + 1 < TT[t]->n) {
-                const int sk = take();
-                if (sk < 0) { ok = false; break; }
-                mma_qk(t, sk);
-                tc5_commit(&bar_empty[sk]);
-              }
+            const int nt = t ? T1.n : T0.n;
+            if (!ok || j >= nt) continue;
+            if (!(ok = wait_p(t, j))) break;
+            const int sv = take();
+            if (sv < 0) { ok = false; break; }
+            mma_pv(t, sv, j > 0);
+            tc5_commit_elect(&bar_empty[sv]);
+            if (j + 1 < nt) {
+              const int sk = take();
+              if (sk < 0) { ok = false; break; }
+              mma_qk(t, sk);
+              tc5_commit_elect(&bar_empty[sk]);
             }
           }
         }
       }
-      // every MMA issued so far has completed before tensor memory is read back or freed
-      tc5_commit(&bar_drain);
-      mbar_wait_drain(&bar_drain, 0, a.timeout_ns);
     }
+    // every MMA issued so far has completed before tensor memory is read back or freed
+    tc5_commit_elect(&bar_drain);
+    mbar_wait_drain(&bar_drain, 0, a.timeout_ns);
   } else {
     // =============================== softmax warpgroups ===============================
     const int t = warp >> 2;                 // tile of this warpgroup
