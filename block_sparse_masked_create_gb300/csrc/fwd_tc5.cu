@@ -32,9 +32,11 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+// 16 softmax warps (2 warpgroups per tile), the TMA producer and the MMA issuer. Five warps share an
+// SM sub-partition, which caps a thread at 96 registers; the softmax fits (it holds 64 scores).
+constexpr int kThreads = 576;
+constexpr int kLoadWarp = 16;
+constexpr int kMmaWarp = 17;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 2^8
@@ -47,10 +49,13 @@ struct Tc5Cfg {
   static constexpr int kSlotBytes = 128 * D * 2;   // one K or V tile
   static constexpr int kStages = D == 128 ? 5 : 12;
   static constexpr int kOffRing = 2 * kQBytes;
-  static constexpr int kSmem = kOffRing + kStages * kSlotBytes + 1024;  // + alignment slack
+  static constexpr int kOffRed = kOffRing + kStages * kSlotBytes;  // float [tile][half][row] exchange
+  static constexpr int kOffBar = kOffRed + 2 * 2 * 128 * 4;        // mbarriers, TMEM address, abort flag
+  static constexpr int kSmem = kOffBar + 512;
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static constexpr uint32_t kTmemCols = 512;
-  // tensor-memory columns: S_t (and P_t over its first 64 columns) at [256 t, 256 t + 128),
-  // O_t at [256 t + 128, 256 t + 128 + D)
+  // tensor-memory columns: S_t at [256 t, 256 t + 128), with P_t (bf16 pairs) over columns [0, 32) and
+  // [64, 96) of it (keys 0..63 and 64..127); O_t at [256 t + 128, 256 t + 128 + D)
   __device__ static constexpr uint32_t col_s(int t) { return (uint32_t)t * 256u; }
   __device__ static constexpr uint32_t col_o(int t) { return (uint32_t)t * 256u + 128u; }
 };
@@ -99,13 +104,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Tc5Cfg<D>;
   constexpr int NST = C::kStages;
   const FwdArgs& a = P.a;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q[2], bar_s[2], bar_p[2], bar_o[2], bar_full[NST], bar_empty[NST], bar_drain;
-  __shared__ uint32_t s_tmem;
-  __shared__ int32_t s_abort;
+  // All shared state is dynamic (no static __shared__), so the buffer starts at the CTA's shared
+  // window and keeps the 1024-byte alignment the 128-byte swizzle needs; checked below, never assumed.
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* const bar_q = bars;          // [2] Q tile landed
+  uint64_t* const bar_s = bars + 2;      // [2] S = Q K^T complete
+  uint64_t* const bar_p = bars + 4;      // [2] P stored in tensor memory (both halves, 256 arrivals)
+  uint64_t* const bar_o = bars + 6;      // [2] O += P V complete
+  uint64_t* const bar_full = bars + 8;   // [NST] ring slot landed
+  uint64_t* const bar_empty = bars + 8 + NST;  // [NST] ring slot consumed
+  uint64_t& bar_drain = bars[8 + 2 * NST];
+  uint32_t& s_tmem = *reinterpret_cast<uint32_t*>(bars + 9 + 2 * NST);
+  int32_t& s_abort = *(reinterpret_cast<int32_t*>(bars + 9 + 2 * NST) + 1);
+  // Half-row maxima of the current block, [tile][half][row]; one buffer suffices: a half writes block
+  // j+1's value only after S(j+1) completed, which the MMA issues only after both halves signalled P(j),
+  // i.e. after both had read block j's values. The epilogue reuses it for the row sums.
+  float (*const s_red)[2][128] = reinterpret_cast<float (*)[2][128]>(smem + C::kOffRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (smem_u32(smem) & 1023u) {  // uniform across the CTA, before any barrier or allocation
+    if (tid == 0) report(a.status, FA_ERR_DEVICE_CHECK);
+    return;
+  }
 
   // ---- work item: (query block r, batch b, head pair hp); heaviest query blocks first for causal
   const int HP = (a.Hq + 1) / 2;
@@ -131,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_q[t], 1);
       mbar_init(&bar_s[t], 1);
-      mbar_init(&bar_p[t], 128);
+      mbar_init(&bar_p[t], 256);
       mbar_init(&bar_o[t], 1);
     }
     for (int s = 0; s < NST; ++s) {
@@ -260,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t vd = vdesc + (uint64_t)(s * (C::kSlotBytes >> 4));
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        tc5_mma_ts_elect(tmem + C::col_o(t), tmem + C::col_s(t) + (uint32_t)(ks * 8), vd + (uint64_t)((ks * 2048) >> 4),
+        tc5_mma_ts_elect(tmem + C::col_o(t), tmem + C::col_s(t) + (uint32_t)(ks * 8 + (ks >= 4 ? 32 : 0)),
+                         vd + (uint64_t)((ks * 2048) >> 4),
                          idesc_pv, (acc || ks > 0) ? 1u : 0u);
       tc5_commit_elect(&bar_o[t]);
     };
@@ -333,8 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_drain(&bar_drain, 0, a.timeout_ns);
   } else {
     // =============================== softmax warpgroups ===============================
-    const int t = warp >> 2;                 // tile of this warpgroup
-    const int row = (warp & 3) * 32 + lane;  // TMEM lane == query row in the tile
+    // Two warpgroups per tile: warpgroup (t, h) owns columns [64 h, 64 h + 64) of the 128 rows of tile t
+    // (TMEM lane == query row == 32 * (warp % 4) + lane). The row maximum is exchanged through shared
+    // memory once per block; the row sums stay per half and are added in the epilogue.
+    const int t = warp >> 3;                 // tile
+    const int h = (warp >> 2) & 1;           // column half
+    const int row = (warp & 3) * 32 + lane;  // query row in the tile
     const Tile TT = t ? T1 : T0;
     uint8_t* const sQt = t ? sQ1 : sQ0;
     const int q_row = r * 128 + row;
@@ -343,14 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_base + C::col_o(t);
     float* Lg = a.lse + ((size_t)b * a.Hq + TT.h) * a.q_len;
     if (TT.valid && TT.n == 0) {
-      // empty query block: O = 0, LSE = -inf, nothing loaded
+      // empty query block: O = 0, LSE = -inf, nothing loaded (each half writes its half of the row)
       const int row_bytes = D * (a.out_f32 ? 4 : 2);
       uint8_t* Ob = reinterpret_cast<uint8_t*>(a.out) + (((size_t)b * a.Hq + TT.h) * a.q_len) * row_bytes;
       if (q_row < a.q_len) {
         const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int c16 = 0; c16 < row_bytes / 16; ++c16)
+        for (int c16 = h * (row_bytes / 32); c16 < (h + 1) * (row_bytes / 32); ++c16)
           *reinterpret_cast<uint4*>(Ob + (size_t)q_row * row_bytes + c16 * 16) = z;
-        Lg[q_row] = -INFINITY;
+        if (h == 0) Lg[q_row] = -INFINITY;
       }
     } else if (TT.valid) {
       const int64_t off_b = a.rule.q_offset ? (int64_t)__ldg(a.rule.q_offset + (M.Bm > 1 ? b : 0)) : 0;
@@ -360,43 +386,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sl2 = a.scale * kLog2e;
       float slope2 = 0.f;
       if (SK == SK_ALIBI || SK == SK_GENERIC) slope2 = a.score.alibi ? __ldg(a.score.alibi + TT.h) * kLog2e : 0.f;
+      const int c_lo = 64 * h;                 // first column of this half within the block
       float m_ref = -INFINITY;  // reference max (log2 domain) used for P and for O
-      float l = 0.f, le = 0.f;
+      float l = 0.f, le = 0.f;  // this half's row sums (rounded P for O, unrounded P for the LSE)
       bool ok = true;
       // tcgen05.ld / st are warp-collective (.sync.aligned): every decision that guards one is made
-      // uniform across the warp (wait results with __all_sync, the O rescale with __any_sync)
-      for (int j = 0; j < TT.n && ok; ++j) {
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_s[t], (uint32_t)(j & 1), wc));
-        if (!ok) break;
+      // uniform across the warp (wait results with __all_sync, the O rescale with __any_sync). The
+      // loop always runs TT.n times so that both halves reach the tile's barrier equally often; after
+      // a failed wait a warp only keeps the barrier count (its waits then return at once).
+      // Each half touches only its own S columns [64 h, 64 h + 64); its P (64 keys as bf16 pairs) goes
+      // over the first 32 of them.
+      for (int j = 0; j < TT.n; ++j) {
+        if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_s[t], (uint32_t)(j & 1), wc));
+        if (!ok) {
+          named_bar_sync(1 + t, 256);
+          continue;
+        }
         tc5_fence_after();
-        float x[128];
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) tc5_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&x[c0]));
+        float x[64];
+        tc5_ld32(tS + c_lo, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+        tc5_ld32(tS + c_lo + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
         tc5_wait_ld();
         const bool partial = j >= TT.n_full;
         const bool need_col = partial || SK != SK_NONE;
         const int c = need_col ? TT.col(j) : 0;
         const int64_t j0 = (int64_t)c * 128;
         // ---- score rule (log2 domain); SK_NONE defers the scale into the exponent's FMA
-        float mult = 1.f;
-        if (SK == SK_NONE) {
-          mult = sl2;
-        } else if (SK == SK_ALIBI) {
-          const float base = -slope2 * (float)(ig - j0);  // bias at column 0 (log2 units)
+        const float mult = SK == SK_NONE ? sl2 : 1.f;
+        if (SK == SK_ALIBI) {
+          const float base = -slope2 * (float)(ig - j0 - c_lo);  // bias at this half's first column
           const uint64_t s2 = f2_pack(sl2, sl2), sp2 = f2_pack(slope2, slope2), b2 = f2_pack(base, base);
 #pragma unroll
-          for (int i = 0; i < 128; i += 2) {
+          for (int i = 0; i < 64; i += 2) {
             const uint64_t bias = f2_fma(sp2, f2_pack((float)i, (float)(i + 1)), b2);
             f2_unpack(f2_fma(f2_pack(x[i], x[i + 1]), s2, bias), x[i], x[i + 1]);
           }
         } else if (SK == SK_SOFTCAP) {
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
+          for (int i = 0; i < 64; ++i)
             x[i] = softcap_apply(x[i] * a.scale, a.score.softcap, a.score.inv_softcap) * kLog2e;
-        } else {
-          for (int i = 0; i < 128; ++i) {
+        } else if (SK == SK_GENERIC) {
+          for (int i = 0; i < 64; ++i) {
             float v = x[i] * a.scale;
-            const int64_t dist = ig - (j0 + i);
+            const int64_t dist = ig - (j0 + c_lo + i);
             if (a.score.alibi) v -= (slope2 * kLn2) * (float)dist;
             if (a.score.rel) {
               int64_t ix = dist + a.score.kv_len - 1;
@@ -420,22 +452,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             });
           }
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t wd = bits.w[k];
+          for (int k = 0; k < 2; ++k) {
+            const uint32_t wd = h ? bits.w[2 + k] : bits.w[k];
 #pragma unroll
             for (int i = 0; i < 32; ++i) x[k * 32 + i] = ((wd >> i) & 1u) ? x[k * 32 + i] : -INFINITY;
           }
         }
-        // ---- row max: 8 independent 3-input max chains
-        float mxk[8];
+        // ---- this half's max: 4 independent 3-input max chains; then the row max across both halves
+        float mxk[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mxk[k] = fmaxf(x[k], x[k + 8]);
+        for (int k = 0; k < 4; ++k) mxk[k] = fmaxf(x[k], x[k + 4]);
 #pragma unroll
-        for (int i = 16; i < 128; i += 16)
+        for (int i = 8; i < 64; i += 8)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) mxk[k] = fmax3(mxk[k], x[i + k], x[i + 8 + k]);
-        const float mb = fmax3(fmax3(mxk[0], mxk[1], mxk[2]), fmax3(mxk[3], mxk[4], mxk[5]), fmaxf(mxk[6], mxk[7])) *
-                         mult;
+          for (int k = 0; k < 4; ++k) mxk[k] = fmax3(mxk[k], x[i + k], x[i + 4 + k]);
+        s_red[t][h][row] = fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3])) * mult;
+        named_bar_sync(1 + t, 256);
+        const float mb = fmaxf(s_red[t][0][row], s_red[t][1][row]);
         // ---- reference max: move it only when the block max exceeds it by more than 2^8
         float alpha = 1.f;
         bool rescale = false;
@@ -446,68 +479,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float mr = m_ref == -INFINITY ? 0.f : m_ref;
         // ---- P = 2^(mult * x - m); two row sums: of the bf16-rounded P the product uses (normalises O:
-        // an exact convex combination of V rows) and of the unrounded P (for the LSE)
+        // an exact convex combination of V rows) and of the unrounded P (for the LSE). P is stored 16
+        // columns (32 keys) at a time.
         const uint64_t mul2 = f2_pack(mult, mult), neg2 = f2_pack(-mr, -mr);
-        uint64_t se[4] = {0, 0, 0, 0}, sr[4] = {0, 0, 0, 0};
-        uint32_t pk[64];
+        uint64_t se[2] = {0, 0}, sr[2] = {0, 0};
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const uint64_t y2 = f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), mul2, neg2);
-          float p0, p1;
-          if ((i & 3) == 3) {  // a quarter of the exponentials on the FMA pipe, the rest on MUFU
-            f2_unpack(f2_exp2_poly(y2), p0, p1);
-          } else {
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
             float y0, y1;
-            f2_unpack(y2, y0, y1);
-            p0 = ex2_approx(y0);
-            p1 = ex2_approx(y1);
+            f2_unpack(f2_fma(f2_pack(x[32 * ch + 2 * i], x[32 * ch + 2 * i + 1]), mul2, neg2), y0, y1);
+            const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+            pk[i] = pack_bf16x2(p0, p1);
+            se[i & 1] = f2_add(se[i & 1], f2_pack(p0, p1));
+            sr[i & 1] = f2_add(sr[i & 1], f2_pack(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xFFFF0000u)));
           }
-          pk[i] = pack_bf16x2(p0, p1);
-          se[i & 3] = f2_add(se[i & 3], f2_pack(p0, p1));
-          sr[i & 3] = f2_add(sr[i & 3], f2_pack(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xFFFF0000u)));
+          tc5_st16(tS + c_lo + 16 * ch, pk);
         }
         float e0, e1, r0, r1;
-        f2_unpack(f2_add(f2_add(se[0], se[1]), f2_add(se[2], se[3])), e0, e1);
-        f2_unpack(f2_add(f2_add(sr[0], sr[1]), f2_add(sr[2], sr[3])), r0, r1);
+        f2_unpack(f2_add(se[0], se[1]), e0, e1);
+        f2_unpack(f2_add(sr[0], sr[1]), r0, r1);
         l = l * alpha + (r0 + r1);
         le = le * alpha + (e0 + e1);
-        // ---- O is stable here: S_t(j) completed, and O_t's previous update was issued before it
+        // ---- O is stable here: S_t(j) completed, and O_t's previous update was issued before it.
+        // Each half rescales its half of O's columns.
         if (__any_sync(0xFFFFFFFFu, rescale)) {
           const float f = rescale ? alpha : 1.f;
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < D / 2; c0 += 32) {
             uint32_t o[32];
-            tc5_ld32(tO + c0, o);
+            tc5_ld32(tO + h * (D / 2) + c0, o);
             tc5_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-            tc5_st32(tO + c0, o);
+            tc5_st32(tO + h * (D / 2) + c0, o);
           }
         }
-        // ---- P into tensor memory over S's first 64 columns (two bf16 per column)
-        tc5_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tc5_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         tc5_wait_st();
         tc5_fence_before();
         mbar_arrive(&bar_p[t]);
       }
-      // ---- epilogue
+      // ---- epilogue: add the two halves' sums, wait for the last O update, normalise and store
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o[t], (uint32_t)((TT.n - 1) & 1), wc));
       tc5_fence_after();
+      // the last O update completed after both halves read the last block's maxima: the exchange
+      // buffer is free for the two sums, one at a time
+      s_red[t][h][row] = l;
+      named_bar_sync(1 + t, 256);
+      const float lt = s_red[t][0][row] + s_red[t][1][row];
+      named_bar_sync(1 + t, 256);
+      s_red[t][h][row] = le;
+      named_bar_sync(1 + t, 256);
+      const float let = s_red[t][0][row] + s_red[t][1][row];
       const bool empty = m_ref == -INFINITY;
-      const float inv = empty ? 0.f : 1.f / l;
-      if (ok && q_row < a.q_len) Lg[q_row] = empty ? -INFINITY : (m_ref + __log2f(le)) * kLn2;
-      // staging in this tile's Q buffer (free: every Q K^T of the tile has completed). bf16: one pass of
-      // D/64 boxes [128][64]; fp32: one pass per 32 columns, each one box [128][32] (128-byte rows).
+      const float inv = empty ? 0.f : 1.f / lt;
+      if (ok && h == 0 && q_row < a.q_len) Lg[q_row] = empty ? -INFINITY : (m_ref + __log2f(let)) * kLn2;
+      // staging in this tile's Q buffer (free: every Q K^T of the tile has completed). bf16: one pass,
+      // D/64 boxes [128][64], each half filling its columns; fp32: one pass per 32 columns (one box
+      // [128][32] of 128-byte rows), filled by the half that owns those columns.
       const int passes = a.out_f32 ? D / 32 : 1;
       for (int ps = 0; ps < passes; ++ps) {
         if (ok) {
           if (!a.out_f32) {
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < D / 2; c0 += 32) {
+              const int cc = h * (D / 2) + c0;
               uint32_t o[32];
-              tc5_ld32(tO + c0, o);
+              tc5_ld32(tO + cc, o);
               tc5_wait_ld();
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) {
@@ -516,10 +556,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
                 v.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
                 v.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
-                *reinterpret_cast<uint4*>(sQt + tile_off(row, c0 / 8 + q4)) = v;
+                *reinterpret_cast<uint4*>(sQt + tile_off(row, cc / 8 + q4)) = v;
               }
             }
-          } else {
+          } else if ((ps * 32) / (D / 2) == h) {
             uint32_t o[32];
             tc5_ld32(tO + ps * 32, o);
             tc5_wait_ld();
@@ -531,11 +571,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        // every thread of the warpgroup reaches these barriers (ok or not); the store runs only if no
-        // role gave up (a failed wait always sets the CTA's abort flag)
+        // every thread of the tile reaches these barriers (ok or not); the store runs only if no role
+        // gave up (a failed wait always sets the CTA's abort flag)
         fence_proxy_async_smem();
-        named_bar_sync(1 + t, 128);
-        if (!*wc.abort && (warp & 3) == 0 && lane == 0) {
+        named_bar_sync(1 + t, 256);
+        if (!*wc.abort && h == 0 && (warp & 3) == 0 && lane == 0) {
           if (!a.out_f32) {
 #pragma unroll
             for (int x = 0; x < D / 64; ++x) tma_store_3d(&tmO, sQt + x * 16384, x * 64, r * 128, b * a.Hq + TT.h);
@@ -545,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_commit_group();
           bulk_wait_group_read0();
         }
-        named_bar_sync(1 + t, 128);  // the staging buffer is free again
+        named_bar_sync(1 + t, 256);  // the staging buffer is free again
       }
     }
   }
