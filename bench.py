@@ -34,6 +34,9 @@ def parse():
     p.add_argument("--workload", default="cfg2", choices=["cfg2", "cfg3", "cfg4"])
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--decode-only", action="store_true",
+                   help="time only the paged decode and print its object as the line (profiling aid)")
+    p.add_argument("--decode-requests", type=int, default=64, help="requests in the decode batch")
     return p.parse_args()
 
 
@@ -372,7 +375,7 @@ def bench_decode(args, dev, pk):
     import torch
 
     from block_sparse_masked_create_gb300 import fa, workloads
-    d = workloads.cfg5().generate()
+    d = workloads.cfg5(Bz=args.decode_requests).generate()
     q = workloads.bf16_torch(d.q_bits, dev)
     kp = workloads.bf16_torch(d.k_bits, dev)
     vp = workloads.bf16_torch(d.v_bits, dev)
@@ -400,7 +403,7 @@ def bench_decode(args, dev, pk):
     other = q.numel() * 2 + out.numel() * 2 + lse.numel() * 4 + pt.numel() * 4
     med = statistics.median(ms)
     gbs = (kv_bytes + other) / (med * 1e-3) / 1e9
-    return {"workload": "cfg5 paged decode: 64 requests, Hq=32, Hkv=8, d=128, 128-token pages, L~U[1024,32768]",
+    return {"workload": f"cfg5 paged decode: {d.Bz} requests, Hq=32, Hkv=8, d=128, 128-token pages, L~U[1024,32768]",
             "kv_gb": kv_bytes / 1e9, "ms_median": med, "GB/s": gbs, "pct_hbm": gbs / pk["hbm"],
             "status": fa.status_string(fa.check_status(status)),
             "note": "KV read once per KV head; K/V pages 2x%.1f GB > L2" % (d.k_bits.nbytes / 1e9)}
@@ -424,6 +427,12 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         reference_arm(args, rank)
+        return
+    if args.decode_only:
+        import torch
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        print(json.dumps(bench_decode(args, dev, peaks())), flush=True)
         return
     ours(args, rank, world, local_rank)
 

@@ -536,18 +536,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool empty = m_ref == -INFINITY;
       const float inv = empty ? 0.f : 1.f / lt;
       if (ok && h == 0 && q_row < a.q_len) Lg[q_row] = empty ? -INFINITY : (m_ref + __log2f(let)) * kLn2;
-      // staging in this tile's Q buffer (free: every Q K^T of the tile has completed). bf16: one pass,
-      // D/64 boxes [128][64], each half filling its columns; fp32: one pass per 32 columns (one box
-      // [128][32] of 128-byte rows), filled by the half that owns those columns.
-      const int passes = a.out_f32 ? D / 32 : 1;
-      for (int ps = 0; ps < passes; ++ps) {
+      // staging in this tile's Q buffer (D/64 sub-buffers of 16 KB; free: every Q K^T of the tile has
+      // completed). bf16: one round of D/64 boxes [128][64], each half filling its columns. fp32: two
+      // rounds of boxes [128][32] (128-byte rows); with D = 128 half h fills sub-buffer h with its
+      // columns 32 rd.. each round, with D = 64 half rd fills the only sub-buffer in round rd.
+      const int rounds = a.out_f32 ? 2 : 1;
+      const bool issuer = h == 0 && (warp & 3) == 0 && lane == 0;
+      for (int rd = 0; rd < rounds; ++rd) {
+        if (rd > 0) {
+          if (issuer) bulk_wait_group_read0();  // the previous round's boxes have left shared memory
+          named_bar_sync(1 + t, 256);
+        }
         if (ok) {
           if (!a.out_f32) {
 #pragma unroll
             for (int c0 = 0; c0 < D / 2; c0 += 32) {
-              const int cc = h * (D / 2) + c0;
               uint32_t o[32];
-              tc5_ld32(tO + cc, o);
+              tc5_ld32(tO + h * (D / 2) + c0, o);
               tc5_wait_ld();
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) {
@@ -556,18 +561,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
                 v.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
                 v.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
-                *reinterpret_cast<uint4*>(sQt + tile_off(row, cc / 8 + q4)) = v;
+                *reinterpret_cast<uint4*>(sQt + tile_off(row, (h * (D / 2) + c0) / 8 + q4)) = v;
               }
             }
-          } else if ((ps * 32) / (D / 2) == h) {
+          } else if (D == 128 || h == rd) {
+            uint8_t* const stg = sQt + (D == 128 ? h * 16384 : 0);
             uint32_t o[32];
-            tc5_ld32(tO + ps * 32, o);
+            tc5_ld32(tO + (D == 128 ? h * 64 + rd * 32 : rd * 32), o);
             tc5_wait_ld();
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
               float4 v = make_float4(__uint_as_float(o[4 * q4 + 0]) * inv, __uint_as_float(o[4 * q4 + 1]) * inv,
                                      __uint_as_float(o[4 * q4 + 2]) * inv, __uint_as_float(o[4 * q4 + 3]) * inv);
-              *reinterpret_cast<float4*>(sQt + row * 128 + ((q4 ^ (row & 7)) << 4)) = v;
+              *reinterpret_cast<float4*>(stg + row * 128 + ((q4 ^ (row & 7)) << 4)) = v;
             }
           }
         }
@@ -575,18 +581,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // gave up (a failed wait always sets the CTA's abort flag)
         fence_proxy_async_smem();
         named_bar_sync(1 + t, 256);
-        if (!*wc.abort && h == 0 && (warp & 3) == 0 && lane == 0) {
+        if (!*wc.abort && issuer) {
           if (!a.out_f32) {
 #pragma unroll
             for (int x = 0; x < D / 64; ++x) tma_store_3d(&tmO, sQt + x * 16384, x * 64, r * 128, b * a.Hq + TT.h);
           } else {
-            tma_store_3d(&tmO, sQt, ps * 32, r * 128, b * a.Hq + TT.h);
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x)
+              tma_store_3d(&tmO, sQt + x * 16384, D == 128 ? x * 64 + rd * 32 : rd * 32, r * 128, b * a.Hq + TT.h);
           }
           bulk_commit_group();
-          bulk_wait_group_read0();
         }
-        named_bar_sync(1 + t, 256);  // the staging buffer is free again
       }
+      // the staging buffer must stay untouched until the last boxes have been read out of it
+      if (issuer) bulk_wait_group_read0();
     }
   }
   tc5_fence_before();
