@@ -179,10 +179,7 @@ __global__ void __launch_bounds__(kDecWarps * 32)
       if (partial) {
         const int w = (int)min((int64_t)kSub, (int64_t)a.mask.kv_len - j0);
         Bits128 bb = rule_row_bits(a.rule, ig, j0, w, doc_i, [&](int d) {
-          Bits128 db = {{0u, 0u, 0u, 0u}};
-          for (int cc = 0; cc < w; ++cc)
-            if (doc_at(a.rule, bm, j0 + cc) == d) db.w[0] |= 1u << cc;
-          return db;
+          return doc_bits<1>(w, d, [&](int c) { return doc_at(a.rule, bm, j0 + c); });
         });
         bits = bb.w[0];
       }

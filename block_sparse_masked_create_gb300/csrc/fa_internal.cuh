@@ -66,6 +66,24 @@ __device__ __forceinline__ int doc_at(const DevRule& R, int b, int64_t pos) {
   return (pos >= 0 && pos < R.doc_len) ? __ldg(row + pos) : -1;
 }
 
+// Bits c < w (of NW 32-bit words) whose column document id coldoc(c) equals d. Fully unrolled with
+// constant word indices, so the words stay in registers.
+template <int NW, class ColDocFn>
+__device__ __forceinline__ Bits128 doc_bits(int w, int d, ColDocFn coldoc) {
+  Bits128 db = {{0u, 0u, 0u, 0u}};
+#pragma unroll
+  for (int k = 0; k < NW; ++k) {
+    uint32_t wd = 0u;
+#pragma unroll
+    for (int b = 0; b < 32; ++b) {
+      const int c = 32 * k + b;
+      if (c < w && coldoc(c) == d) wd |= 1u << b;
+    }
+    db.w[k] = wd;
+  }
+  return db;
+}
+
 // Allowed bits of one query row (global position ig) over KV columns [j0, j0 + w), w <= 128.
 // `docbits(d)` returns the bits of columns whose document id equals d (only called if R.any_doc).
 template <class DocBitsFn>

@@ -169,12 +169,7 @@ __global__ void __launch_bounds__(MmaCfg<D, BQ, BK>::kThreads)
     Bits128 bits_a = {{~0u, ~0u, ~0u, ~0u}}, bits_b = bits_a;
     if (partial) {
       const int w = min(BK, a.kv_len - j0);
-      auto docbits = [&](int d) {
-        Bits128 db = {{0u, 0u, 0u, 0u}};
-        for (int cc = 0; cc < w; ++cc)
-          if (sDoc[cc] == d) db.w[cc >> 5] |= 1u << (cc & 31);
-        return db;
-      };
+      auto docbits = [&](int d) { return doc_bits<(BK + 31) / 32>(w, d, [&](int c) { return sDoc[c]; }); };
       bits_a = row_a < a.q_len ? rule_row_bits(a.rule, ig_a, j0, w, doc_a, docbits) : Bits128{{0u, 0u, 0u, 0u}};
       bits_b = row_b < a.q_len ? rule_row_bits(a.rule, ig_b, j0, w, doc_b, docbits) : Bits128{{0u, 0u, 0u, 0u}};
     }

@@ -441,19 +441,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- mask after the score rule, partial blocks only
         if (partial) {
-          const int w = (int)min((int64_t)128, (int64_t)a.kv_len - j0);
+          // this half's 64 columns only
+          const int64_t jh = j0 + c_lo;
+          const int w = (int)max((int64_t)0, min((int64_t)64, (int64_t)a.kv_len - jh));
           Bits128 bits = {{0u, 0u, 0u, 0u}};
-          if (q_row < a.q_len) {
-            bits = rule_row_bits(a.rule, ig, j0, w, doc_i, [&](int dq) {
-              Bits128 db = {{0u, 0u, 0u, 0u}};
-              for (int cc = 0; cc < w; ++cc)
-                if (doc_at(a.rule, bm, j0 + cc) == dq) db.w[cc >> 5] |= 1u << (cc & 31);
-              return db;
+          if (q_row < a.q_len && w > 0) {
+            bits = rule_row_bits(a.rule, ig, jh, w, doc_i, [&](int dq) {
+              return doc_bits<2>(w, dq, [&](int cc) { return doc_at(a.rule, bm, jh + cc); });
             });
           }
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
-            const uint32_t wd = h ? bits.w[2 + k] : bits.w[k];
+            const uint32_t wd = bits.w[k];
 #pragma unroll
             for (int i = 0; i < 32; ++i) x[k * 32 + i] = ((wd >> i) & 1u) ? x[k * 32 + i] : -INFINITY;
           }

@@ -2,12 +2,15 @@
 // "building the table from mask_mod": evaluate the rule inside every block, reduce any/all, compact to
 // indices; the query-side transpose of section 2.1).
 //
-// Kernel 1 (one CTA per (b_m, h_m, query block r)): every thread owns one query row of the block and
-// evaluates the rule as a 128-bit vector per KV block (interval arithmetic per OR-term, document ids
-// compared per column only when the rule reads them). Rows vote "some pair allowed" / "some pair not
-// allowed" per KV block; a CTA-wide prefix sum then compacts the partial and full column ids in
-// ascending order and zero-fills the unused slots.
+// Kernel 1 (one CTA per (b_m, h_m, query block r)): each KV block is first classified from the rule's
+// terms at block level (interval tests, document-id ranges); only the blocks that test cannot decide
+// are visited pair by pair: every thread owns one query row and evaluates the rule as a 128-bit vector
+// over the block's columns (interval arithmetic per OR-term, document ids compared per column), rows
+// vote "some pair allowed" / "some pair not allowed". A CTA-wide prefix sum then compacts the partial
+// and full column ids in ascending order and zero-fills the unused slots.
 // Kernel 2 (one CTA per (b_m, h_m, KV block c)): the same compaction down a column of the class matrix.
+#include <climits>
+
 #include "fa_launch.h"
 
 namespace fa {
@@ -15,7 +18,7 @@ namespace fa {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kChunk = 4096;  // KV (or query) blocks classified per pass of a CTA
+constexpr int kChunk = 2048;  // KV (or query) blocks classified per pass of a CTA
 
 struct ScanOut {
   int excl_a, excl_b, tot_a, tot_b;
@@ -58,63 +61,196 @@ __device__ __forceinline__ ScanOut block_scan2(int a, int b, int* s_tmp /* [8] *
   return r;
 }
 
+constexpr uint8_t kUnknown = 0xFF;  // class not decided by the block-level test
+constexpr int kDocStage = 4096;     // column document ids staged in shared memory per visiting round
+
+// Min / max over the CTA (128 threads) of two values.
+__device__ __forceinline__ void block_minmax(int& mn, int& mx, int* s_tmp /* [8] */) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  }
+  if (lane == 0) {
+    s_tmp[warp] = mn;
+    s_tmp[4 + warp] = mx;
+  }
+  __syncthreads();
+  mn = min(min(s_tmp[0], s_tmp[1]), min(s_tmp[2], s_tmp[3]));
+  mx = max(max(s_tmp[4], s_tmp[5]), max(s_tmp[6], s_tmp[7]));
+  __syncthreads();
+}
+
+// Class of block (rows [g0, g1) in global positions, all of the query block's valid rows; columns
+// [j0, j1)) decided from the rule's terms without visiting pairs. Per term the columns allowed by
+// "j < pre" form an interval and causal / window bound d = i - j to an interval; over a rectangle of
+// rows x columns d takes every integer between its extremes, so "some pair" and "every pair" are
+// exact interval tests. Document equality is decided only when the row and column document ranges
+// are disjoint (no equal pair) or both a single equal id (always equal); otherwise, and for an OR of
+// terms none of which covers the block alone, the answer is kUnknown and the caller visits the pairs.
+__device__ __forceinline__ uint8_t classify_block(const DevRule& R, int64_t g0, int64_t g1, int64_t j0, int64_t j1,
+                                                  bool full_shape, int rdmin, int rdmax, int cdmin, int cdmax) {
+  if (g1 <= g0 || j1 <= j0) return FA_BLOCK_EMPTY;
+  bool any = false, all = false, unknown = false;
+  for (int t = 0; t < R.n_terms; ++t) {
+    const DevTerm T = R.t[t];
+    const int64_t jhi = T.pre != INT64_MAX ? min(j1, T.pre) : j1;
+    if (jhi <= j0) continue;  // no column of the block is allowed by this term
+    const bool all_j = T.pre == INT64_MAX || j1 <= T.pre;
+    const int64_t dlo = T.causal ? 0 : INT64_MIN;
+    const int64_t dhi = T.win != INT64_MAX ? T.win - 1 : INT64_MAX;
+    bool any_t = !((g1 - 1) - j0 < dlo || g0 - (jhi - 1) > dhi);
+    bool all_t = all_j && g0 - (j1 - 1) >= dlo && (g1 - 1) - j0 <= dhi;
+    if (T.doc) {
+      if (cdmax < rdmin || cdmin > rdmax) {
+        any_t = all_t = false;
+      } else if (!(rdmin == rdmax && cdmin == cdmax)) {
+        all_t = false;
+        if (any_t) {
+          unknown = true;
+          any_t = false;
+        }
+      }
+    }
+    any = any || any_t;
+    all = all || all_t;
+  }
+  if (!full_shape) return any ? FA_BLOCK_PARTIAL : (unknown ? kUnknown : FA_BLOCK_EMPTY);
+  if (all) return FA_BLOCK_FULL;
+  if (unknown) return kUnknown;
+  if (!any) return FA_BLOCK_EMPTY;
+  return R.n_terms > 1 ? kUnknown : FA_BLOCK_PARTIAL;
+}
+
 __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, MaskOut T) {
   const int r = blockIdx.x, hm = blockIdx.y, bm = blockIdx.z;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Bq = T.bq, Bk = T.bk, nk = T.nk;
-  const int lanes = kThreads / Bq;  // KV blocks evaluated side by side
+  const int64_t off = R.q_offset ? (int64_t)__ldg(R.q_offset + bm) : 0;
+  const int64_t i0 = (int64_t)r * Bq, i1 = min(i0 + Bq, (int64_t)T.q_len);  // valid rows [i0, i1)
+  const bool rows_full = i1 - i0 == Bq;
+
+  __shared__ uint8_t s_cls[kChunk];
+  __shared__ int s_a[kChunk];  // column-block document minimum, then "some pair allowed"
+  __shared__ int s_b[kChunk];  // column-block document maximum, then "some pair not allowed"
+  __shared__ int s_tmp[8];
+  __shared__ int s_doc[kDocStage];  // column document ids of the blocks visited side by side
+
+  // document range of the query block's valid rows
+  int rdmin = INT_MAX, rdmax = INT_MIN;
+  if (R.any_doc) {
+    for (int64_t i = i0 + tid; i < i1; i += kThreads) {
+      const int d = doc_at(R, bm, i + off);
+      rdmin = min(rdmin, d);
+      rdmax = max(rdmax, d);
+    }
+    block_minmax(rdmin, rdmax, s_tmp);
+  }
+
+  // per-row state of the exact evaluation (row rho of lam-th block evaluated side by side)
+  const int lanes = kThreads / Bq;
   const int rho = tid % Bq, lam = tid / Bq;
   const bool active = lam < lanes;
-  const int64_t i = (int64_t)r * Bq + rho;
+  const int64_t i = i0 + rho;
   const bool row_in = active && i < T.q_len;
-  const int64_t ig = i + (R.q_offset ? (int64_t)__ldg(R.q_offset + bm) : 0);
+  const int64_t ig = i + off;
   const int doc_i = (R.any_doc && row_in) ? doc_at(R, bm, ig) : -1;
-
-  __shared__ uint8_t s_any[kChunk];
-  __shared__ uint8_t s_notall[kChunk];
-  __shared__ int s_tmp[8];
+  const Bits128 full_bk = range_bits(0, Bk);
 
   const size_t row = ((size_t)bm * T.Hm + hm) * T.nq + r;
   int32_t* kv_idx = T.kv_idx + row * nk;
   int32_t* full_idx = T.full_kv_idx + row * nk;
   uint8_t* cls_row = T.block_class + row * nk;
-  const Bits128 full_bk = range_bits(0, Bk);
 
   int run_p = 0, run_f = 0;
   for (int c0 = 0; c0 < nk; c0 += kChunk) {
     const int cn = min(kChunk, nk - c0);
-    for (int x = tid; x < cn; x += kThreads) {
-      s_any[x] = 0;
-      s_notall[x] = 0;
-    }
-    __syncthreads();
-    if (active) {
-      for (int cc = lam; cc < cn; cc += lanes) {
-        const int64_t j0 = (int64_t)(c0 + cc) * Bk;
+    // 1. document range of every column block of the chunk (a warp per block, coalesced)
+    if (R.any_doc) {
+      for (int x = warp; x < cn; x += kThreads / 32) {
+        const int64_t j0 = (int64_t)(c0 + x) * Bk;
         const int w = (int)min((int64_t)Bk, (int64_t)T.kv_len - j0);
-        bool any = false, all = false;
-        if (row_in) {
-          Bits128 b = rule_row_bits(R, ig, j0, w, doc_i, [&](int d) {
-            Bits128 db = {{0u, 0u, 0u, 0u}};
-            for (int c = 0; c < w; ++c)
-              if (doc_at(R, bm, j0 + c) == d) db.w[c >> 5] |= 1u << (c & 31);
-            return db;
-          });
-          any = (b.w[0] | b.w[1] | b.w[2] | b.w[3]) != 0u;
-          all = (w == Bk) && b.w[0] == full_bk.w[0] && b.w[1] == full_bk.w[1] && b.w[2] == full_bk.w[2] &&
-                b.w[3] == full_bk.w[3];
+        int mn = INT_MAX, mx = INT_MIN;
+        for (int cc = lane; cc < w; cc += 32) {
+          const int d = doc_at(R, bm, j0 + cc);
+          mn = min(mn, d);
+          mx = max(mx, d);
         }
-        if (any) s_any[cc] = 1;
-        if (!all) s_notall[cc] = 1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+          mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        }
+        if (lane == 0) {
+          s_a[x] = mn;
+          s_b[x] = mx;
+        }
       }
+      __syncthreads();
+    }
+    // 2. block-level classification
+    bool has_unknown = false;
+    for (int x = tid; x < cn; x += kThreads) {
+      const int64_t j0 = (int64_t)(c0 + x) * Bk, j1 = min(j0 + Bk, (int64_t)T.kv_len);
+      const uint8_t cl = classify_block(R, i0 + off, i1 + off, j0, j1, rows_full && j1 - j0 == Bk, rdmin, rdmax,
+                                        R.any_doc ? s_a[x] : 0, R.any_doc ? s_b[x] : 0);
+      s_cls[x] = cl;
+      has_unknown = has_unknown || cl == kUnknown;
+    }
+    // 3. undecided blocks: every valid row evaluates the rule over the block's columns
+    if (__syncthreads_or(has_unknown)) {
+      for (int x = tid; x < cn; x += kThreads) {
+        s_a[x] = 0;
+        s_b[x] = 0;
+      }
+      __syncthreads();
+      // rounds of `lanes` blocks side by side; the blocks' column document ids are staged in shared
+      // memory when they fit (every thread of the CTA takes part in the rounds and their barriers)
+      const bool stage = R.any_doc && lanes * Bk <= kDocStage;
+      for (int base = 0; base < cn; base += lanes) {
+        bool round_has = false;  // same answer in every thread (s_cls is stable here)
+        for (int l = 0; l < lanes && base + l < cn; ++l) round_has = round_has || s_cls[base + l] == kUnknown;
+        if (!round_has) continue;
+        if (stage) {
+          for (int x = tid; x < lanes * Bk; x += kThreads) {
+            const int cc = base + x / Bk;
+            const int64_t j = (int64_t)(c0 + cc) * Bk + x % Bk;
+            s_doc[x] = (cc < cn && s_cls[cc] == kUnknown && j < T.kv_len) ? doc_at(R, bm, j) : 0;
+          }
+          __syncthreads();
+        }
+        const int cc = base + lam;
+        if (active && cc < cn && s_cls[cc] == kUnknown) {
+          const int64_t j0 = (int64_t)(c0 + cc) * Bk;
+          const int w = (int)min((int64_t)Bk, (int64_t)T.kv_len - j0);
+          bool any = false, all = false;
+          if (row_in) {
+            const int* cdoc = s_doc + lam * Bk;
+            Bits128 b = rule_row_bits(R, ig, j0, w, doc_i, [&](int d) {
+              return stage ? doc_bits<4>(w, d, [&](int c) { return cdoc[c]; })
+                           : doc_bits<4>(w, d, [&](int c) { return doc_at(R, bm, j0 + c); });
+            });
+            any = (b.w[0] | b.w[1] | b.w[2] | b.w[3]) != 0u;
+            all = (w == Bk) && b.w[0] == full_bk.w[0] && b.w[1] == full_bk.w[1] && b.w[2] == full_bk.w[2] &&
+                  b.w[3] == full_bk.w[3];
+          }
+          if (any) s_a[cc] = 1;
+          if (!all) s_b[cc] = 1;
+        }
+        if (stage) __syncthreads();
+      }
+      __syncthreads();
+      for (int x = tid; x < cn; x += kThreads)
+        if (s_cls[x] == kUnknown) s_cls[x] = s_a[x] ? (s_b[x] ? FA_BLOCK_PARTIAL : FA_BLOCK_FULL) : FA_BLOCK_EMPTY;
     }
     __syncthreads();
-    // classify the chunk and compact (each thread owns a contiguous segment -> ascending order)
+    // 4. compaction (each thread owns a contiguous segment -> ascending order)
     const int seg = (cn + kThreads - 1) / kThreads;
     const int s0 = min(tid * seg, cn), s1 = min(s0 + seg, cn);
     int np = 0, nf = 0;
     for (int x = s0; x < s1; ++x) {
-      const uint8_t cl = s_any[x] ? (s_notall[x] ? FA_BLOCK_PARTIAL : FA_BLOCK_FULL) : FA_BLOCK_EMPTY;
+      const uint8_t cl = s_cls[x];
       cls_row[c0 + x] = cl;
       np += cl == FA_BLOCK_PARTIAL;
       nf += cl == FA_BLOCK_FULL;
@@ -122,9 +258,9 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
     ScanOut so = block_scan2(np, nf, s_tmp);
     int p = run_p + so.excl_a, f = run_f + so.excl_b;
     for (int x = s0; x < s1; ++x) {
-      const bool a = s_any[x] != 0, na = s_notall[x] != 0;
-      if (a && na) kv_idx[p++] = c0 + x;
-      if (a && !na) full_idx[f++] = c0 + x;
+      const uint8_t cl = s_cls[x];
+      if (cl == FA_BLOCK_PARTIAL) kv_idx[p++] = c0 + x;
+      if (cl == FA_BLOCK_FULL) full_idx[f++] = c0 + x;
     }
     run_p += so.tot_a;
     run_f += so.tot_b;

@@ -71,6 +71,18 @@ def test_rule_sweep_ragged(ri, q_len, kv_len, bq, bk):
     assert_tables_equal(t, want)
 
 
+@pytest.mark.parametrize("ri", [7, 8, 9])
+@pytest.mark.parametrize("q_len,kv_len,bq,bk,ndoc", [(130, 130, 16, 16, 3), (256, 256, 64, 128, 40), (77, 200, 8, 4, 2)])
+def test_rule_sweep_unsorted_docs(ri, q_len, kv_len, bq, bk, ndoc):
+    # document ids in no particular order: row and column id ranges overlap in most blocks, so the
+    # builder must visit pairs to tell partial from empty and full
+    spec = RULES[ri]
+    rng = np.random.default_rng(1000 * ri + q_len + ndoc)
+    doc = rng.integers(0, ndoc, size=(1, max(q_len, kv_len))).astype(np.int32)
+    _, t = gpu_tables(spec, 1, 1, q_len, kv_len, bq, bk, doc=doc)
+    assert_tables_equal(t, orc.block_mask(spec, 1, 1, q_len, kv_len, bq, bk, doc_ids=doc))
+
+
 def test_batch_dependent_offsets_and_docs():
     B, H = 3, 2
     off = np.array([0, 17, 40], dtype=np.int32)
