@@ -157,6 +157,21 @@ print(json.dumps({"times": times, "flops": flops}))
 """
 
 
+def max_over_ranks(ms: float, dist=None, device=None) -> float:
+    """The job's time is the slowest rank's: all-reduce MAX of each rank's timed region (ms)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flop_per_rank: float, ms_step: float) -> float:
+    """Whole-job throughput: every rank processes its own shard of flop_per_rank per step (weak scaling)."""
+    return world * flop_per_rank / (ms_step * 1e-3) / 1e12
+
+
 def run_oracle_sample(wl: str, reps: int) -> dict:
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
@@ -277,16 +292,12 @@ def ours(args, rank, world, local_rank):
         clk.busy_for(busy, 0.5)
     if dist:
         dist.barrier()
-    ms = start.elapsed_time(end)
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(start.elapsed_time(end), dist, dev)
     fwd_ms = [a.elapsed_time(c) for (_, a, c) in ev]
     mask_ms = [s.elapsed_time(a) for (s, a, _) in ev]
     st_code = fa.check_status(status)
     ms_step = ms / args.steps
-    value = world * phys_flops / (ms_step * 1e-3) / 1e12
+    value = job_tflops(world, phys_flops, ms_step)
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
     achieved = phys_flops / (fwd_avg * 1e-3) / 1e12
 
@@ -410,11 +421,19 @@ def bench_decode(args, dev, pk):
 
 
 def load_traffic(wl):
-    """dram bytes per launch of the forward kernel from the committed ncu summary, if it matches."""
+    """DRAM bytes per launch of the forward kernel from the committed ncu capture, or None when there is no
+    capture for this workload or the kernel's sources changed since it was taken."""
+    import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             t = json.load(f)
+        h = hashlib.sha1()
+        for name in ("fwd_tc5.cu", "fa_internal.cuh"):
+            with open(os.path.join(ROOT, "block_sparse_masked_create_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != t.get("source_sha1"):
+            return None
         return t.get(wl)
     except Exception:
         return None
