@@ -40,6 +40,7 @@ constexpr int kMmaWarp = 17;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 2^8
+constexpr int kGroupPairs = 8;             // (batch, head pair) units sharing the L2 at a time
 
 enum ScoreKind { SK_NONE = 0, SK_ALIBI = 1, SK_SOFTCAP = 2, SK_GENERIC = 3 };
 
@@ -128,14 +129,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  // ---- work item: (query block r, batch b, head pair hp); heaviest query blocks first for causal
+  // ---- work item: (query block r, batch b, head pair hp). The (b, hp) pairs are taken in groups of
+  // kGroupPairs; within a group the query blocks go from the last to the first (heaviest first for causal
+  // masks) with the group's pairs side by side, so the CTAs resident at any time share the K / V of a
+  // few heads in L2 instead of streaming every head's K / V from DRAM once per query block.
   const int HP = (a.Hq + 1) / 2;
   const DevMask& M = a.mask;
-  int p = blockIdx.x;
-  const int hp = p % HP;
-  p /= HP;
-  const int b = p % a.B;
-  const int r = M.nq - 1 - p / a.B;
+  const int NP = a.B * HP;
+  const int GS = NP < kGroupPairs ? NP : kGroupPairs;
+  const int g = blockIdx.x / (GS * M.nq), g0 = g * GS, gs = min(GS, NP - g0);
+  const int rem = blockIdx.x - g * GS * M.nq;
+  const int pair = g0 + rem % gs;
+  const int hp = pair % HP;
+  const int b = pair / HP;
+  const int r = M.nq - 1 - rem / gs;
   const Tile T0 = make_tile(a, b, 2 * hp, r);
   const Tile T1 = make_tile(a, b, 2 * hp + 1, r);
   // sibling heads of one KV head with the same mask row share K / V loads
