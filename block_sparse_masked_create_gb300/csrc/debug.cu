@@ -139,6 +139,11 @@ __global__ void __launch_bounds__(128) debug_tc5_gemm_kernel(const __nv_bfloat16
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+__global__ void debug_softcap_kernel(const float* x, float* y, int n, float c) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) y[i] = softcap_apply(x[i], c, 1.0f / c);
+}
+
 __global__ void debug_exp2_kernel(const float* x, float* y_poly, float* y_mufu, int n) {
   const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
   if (i >= n) return;
@@ -161,6 +166,12 @@ cudaError_t launch_debug_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t
 }
 
 }  // namespace fa
+
+extern "C" fa_status fa_debug_softcap(const float* x, float* y, int32_t n, float c, fa_stream_t stream) {
+  if (!x || !y || n < 1 || !(c > 0.f)) return FA_ERR_INVALID_ARG;
+  fa::debug_softcap_kernel<<<(n + 255) / 256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(x, y, n, c);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 extern "C" fa_status fa_debug_exp2(const float* x, float* y_poly, float* y_mufu, int32_t n, fa_stream_t stream) {
   if (!x || !y_poly || !y_mufu || n < 1) return FA_ERR_INVALID_ARG;

@@ -429,9 +429,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             f2_unpack(f2_fma(f2_pack(x[i], x[i + 1]), s2, bias), x[i], x[i + 1]);
           }
         } else if (SK == SK_SOFTCAP) {
+          // log2(e) c tanh(scale x / c), packed multiplies around the tanh
+          const float ain = a.scale * a.score.inv_softcap, aout = a.score.softcap * kLog2e;
+          const uint64_t in2 = f2_pack(ain, ain), out2 = f2_pack(aout, aout);
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
-            x[i] = softcap_apply(x[i] * a.scale, a.score.softcap, a.score.inv_softcap) * kLog2e;
+          for (int i = 0; i < 64; i += 2) {
+            float u0, u1;
+            f2_unpack(f2_mul(f2_pack(x[i], x[i + 1]), in2), u0, u1);
+            f2_unpack(f2_mul(f2_pack(tanh_approx(u0), tanh_approx(u1)), out2), x[i], x[i + 1]);
+          }
         } else if (SK == SK_GENERIC) {
           for (int i = 0; i < 64; ++i) {
             float v = x[i] * a.scale;

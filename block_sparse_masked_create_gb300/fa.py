@@ -103,6 +103,8 @@ def load() -> ctypes.CDLL:
     lib.fa_debug_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
     lib.fa_debug_exp2.restype = ctypes.c_int
     lib.fa_debug_exp2.argtypes = [vp, vp, vp, i32, vp]
+    lib.fa_debug_softcap.restype = ctypes.c_int
+    lib.fa_debug_softcap.argtypes = [vp, vp, i32, ctypes.c_float, vp]
     lib.fa_debug_tc5_gemm.restype = ctypes.c_int
     lib.fa_debug_tc5_gemm.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
     _lib = lib
@@ -345,6 +347,13 @@ def debug_exp2(x: torch.Tensor):
     ym = torch.empty_like(x)
     _check(load().fa_debug_exp2(_ptr(x), _ptr(yp), _ptr(ym), x.numel(), _stream(x.device)), "fa_debug_exp2")
     return yp, ym
+
+
+def debug_softcap(x: torch.Tensor, c: float) -> torch.Tensor:
+    """c * tanh(x / c) as the kernels compute it, for a contiguous fp32 CUDA tensor."""
+    y = torch.empty_like(x)
+    _check(load().fa_debug_softcap(_ptr(x), _ptr(y), x.numel(), float(c), _stream(x.device)), "fa_debug_softcap")
+    return y
 
 
 def debug_tc5_gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, K: int, b_mn_major: bool, use_tma: bool,

@@ -260,6 +260,10 @@ FA_API fa_status fa_debug_tc5_gemm(const void* A, const void* B, float* C, int32
  * x, y_poly, y_mufu: device fp32 [n]. */
 FA_API fa_status fa_debug_exp2(const float* x, float* y_poly, float* y_mufu, int32_t n, fa_stream_t stream);
 
+/* Self-test of the soft-cap every kernel applies: y[i] = c * tanh(x[i] / c) ("5.1.2 FlexAttention: from
+ * rules to fused kernels", section 1.2). x, y: device fp32 [n]; c > 0. */
+FA_API fa_status fa_debug_softcap(const float* x, float* y, int32_t n, float c, fa_stream_t stream);
+
 /* Library version string. */
 FA_API const char* fa_version(void);
 

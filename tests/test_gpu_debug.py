@@ -34,6 +34,21 @@ def test_exp2_polynomial_error_bound():
     assert zc[0] == 0.0 and 0.0 <= zc[1] < 1e-37 and abs(zc[2] - 1.0) < 1e-4 and abs(zc[3] - 2.0) < 2e-4
 
 
+@pytest.mark.parametrize("c", [20.0, 50.0])
+def test_softcap_error_bound(c):
+    # the kernels' soft-cap against fp64 c * tanh(x / c), over scores far beyond the cap
+    x = torch.cat([torch.linspace(-8 * c, 8 * c, 1 << 20, dtype=torch.float64),
+                   torch.randn(1 << 16, dtype=torch.float64) * 4.0]).float().cuda()
+    y = fa.debug_softcap(x, c)
+    ref = c * torch.tanh(x.double() / c)
+    err = (y.double() - ref).abs()
+    assert err.max().item() < c * 2e-5, err.max().item()
+    small = x.abs() < c / 2
+    rel = (err[small] / ref[small].abs().clamp_min(1e-30)).max().item()
+    assert rel < 3e-5, rel
+    assert bool((y.abs() <= c).all())
+
+
 @pytest.mark.parametrize("K", [64, 128])
 @pytest.mark.parametrize("b_mn", [False, True])
 @pytest.mark.parametrize("use_tma", [0, 1, 2], ids=["st", "tma", "a_tmem"])
