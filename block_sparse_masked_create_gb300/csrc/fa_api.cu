@@ -92,6 +92,8 @@ static int compile_rule(const fa_mask_rule* r, DevRule* out) {
     out->doc_batch = r->doc_batch;
     out->doc_len = r->doc_len;
     out->q_offset = r->q_offset;
+    out->doc_run = nullptr;
+    out->doc_sorted = nullptr;
   }
   return FA_OK;
 }
@@ -130,9 +132,15 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct MaskLayout {
   int Bm, Hm, nq, nk;
-  size_t off[9];
+  size_t off[11];  // the nine tables, then document run bounds and sortedness flags (document rules)
   size_t total;
 };
+
+static bool rule_reads_doc(const fa_mask_rule* r) {
+  for (int i = 0; i < r->n_ops && i < FA_MAX_RULE_OPS; ++i)
+    if (r->op[i] == FA_M_DOC) return true;
+  return false;
+}
 
 static int mask_layout(const fa_mask_rule* rule, int B, int H, int Q_LEN, int KV_LEN, int Bq, int Bk,
                        MaskLayout* L) {
@@ -146,9 +154,12 @@ static int mask_layout(const fa_mask_rule* rule, int B, int H, int Q_LEN, int KV
   const size_t heads = (size_t)L->Bm * L->Hm;
   const size_t rowsz = heads * L->nq * sizeof(int32_t), colsz = heads * L->nk * sizeof(int32_t);
   const size_t grid = heads * (size_t)L->nq * L->nk;
-  const size_t sizes[9] = {rowsz, rowsz, colsz, colsz, grid * 4, grid * 4, grid * 4, grid * 4, grid};
+  const bool doc = rule_reads_doc(rule) && rule->doc_len > 0 && rule->doc_batch > 0;
+  const size_t nb = doc ? (size_t)rule->doc_batch : 0, dl = doc ? (size_t)rule->doc_len : 0;
+  const size_t sizes[11] = {rowsz, rowsz, colsz, colsz, grid * 4, grid * 4, grid * 4, grid * 4, grid,
+                            nb * 2 * dl * sizeof(int32_t), nb * sizeof(int32_t)};
   size_t o = 0;
-  for (int i = 0; i < 9; ++i) {
+  for (int i = 0; i < 11; ++i) {
     L->off[i] = o;
     o += align256(sizes[i]);
   }
@@ -235,6 +246,8 @@ static int forward_impl(bool force_mma, const void* q, const void* k, const void
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
   s = compile_rule(&bm->rule, &a.rule);
+  a.rule.doc_run = bm->doc_run;
+  a.rule.doc_sorted = bm->doc_sorted;
   if (s != FA_OK) return s;
   a.q = q;
   a.k = k;
@@ -330,6 +343,8 @@ fa_status fa_create_block_mask(const fa_mask_rule* rule, int32_t B, int32_t H, i
   T.q_idx = reinterpret_cast<int32_t*>(base + L.off[6]);
   T.full_q_idx = reinterpret_cast<int32_t*>(base + L.off[7]);
   T.block_class = base + L.off[8];
+  T.doc_run = R.any_doc ? reinterpret_cast<int32_t*>(base + L.off[9]) : nullptr;
+  T.doc_sorted = R.any_doc ? reinterpret_cast<int32_t*>(base + L.off[10]) : nullptr;
   if (L.Hm > 65535 || L.Bm > 65535 || L.nq > INT_MAX / 2 || L.nk > 65535 * 1024) return FA_ERR_UNSUPPORTED;
   if (launch_mask_build(R, T, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   out->Bm = T.Bm;
@@ -349,6 +364,8 @@ fa_status fa_create_block_mask(const fa_mask_rule* rule, int32_t B, int32_t H, i
   out->full_q_num = T.full_q_num;
   out->full_q_idx = T.full_q_idx;
   out->block_class = T.block_class;
+  out->doc_run = T.doc_run;
+  out->doc_sorted = T.doc_sorted;
   out->rule = *rule;
   return FA_OK;
 }
@@ -400,6 +417,8 @@ fa_status fa_flex_decode(const void* q, const void* k_pages, const void* v_pages
   DecArgs a;
   std::memset(&a, 0, sizeof(a));
   int s = compile_rule(&bm->rule, &a.rule);
+  a.rule.doc_run = bm->doc_run;
+  a.rule.doc_sorted = bm->doc_sorted;
   if (s != FA_OK) return (fa_status)s;
   a.q = q;
   a.k_pages = k_pages;

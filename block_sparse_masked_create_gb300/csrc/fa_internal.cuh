@@ -35,6 +35,12 @@ struct DevRule {
   int32_t doc_batch;
   int32_t doc_len;
   const int32_t* q_offset;
+  // run bounds of the document ids, filled by the block-mask builder: doc_run [doc_batch][2][doc_len]
+  // holds, per position, the first and one-past-last position of the run of equal ids around it;
+  // doc_sorted [doc_batch] is 1 where the ids never decrease (then every id is one run, and document
+  // equality with position p is exactly the column interval of p's run). NULL: not available.
+  const int32_t* doc_run;
+  const int32_t* doc_sorted;
 };
 
 struct Bits128 {
@@ -64,6 +70,19 @@ __device__ __forceinline__ int clamp_rel(int64_t x, int w) {
 __device__ __forceinline__ int doc_at(const DevRule& R, int b, int64_t pos) {
   const int32_t* row = R.doc_ids + (int64_t)(R.doc_batch > 1 ? b : 0) * R.doc_len;
   return (pos >= 0 && pos < R.doc_len) ? __ldg(row + pos) : -1;
+}
+
+// Whether document equality of batch row b can be read from run bounds (ids non-decreasing).
+__device__ __forceinline__ bool doc_runs_usable(const DevRule& R, int b) {
+  return R.doc_run != nullptr && __ldg(R.doc_sorted + (R.doc_batch > 1 ? b : 0)) != 0;
+}
+
+// Positions [lo, hi) holding the same document id as position pos, for pos inside the id array (a
+// position outside has id -1, which the caller compares id by id instead) and doc_runs_usable.
+__device__ __forceinline__ void doc_run_of(const DevRule& R, int b, int64_t pos, int64_t& lo, int64_t& hi) {
+  const int32_t* run = R.doc_run + (int64_t)(R.doc_batch > 1 ? b : 0) * 2 * R.doc_len;
+  lo = __ldg(run + pos);
+  hi = __ldg(run + R.doc_len + pos);
 }
 
 // Bits c < w (of NW 32-bit words) whose column document id coldoc(c) equals d. Fully unrolled with

@@ -29,6 +29,8 @@ struct MaskOut {
   int32_t* full_q_num;
   int32_t* full_q_idx;
   uint8_t* block_class;
+  int32_t* doc_run;     // [doc_batch][2][doc_len] or NULL
+  int32_t* doc_sorted;  // [doc_batch] or NULL
 };
 
 cudaError_t launch_mask_build(const DevRule& R, const MaskOut& T, cudaStream_t st);

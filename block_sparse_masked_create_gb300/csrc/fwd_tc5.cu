@@ -390,6 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t ig = (int64_t)q_row + off_b;
       const int bm = M.Bm > 1 ? b : 0;
       const int doc_i = a.rule.any_doc ? doc_at(a.rule, bm, ig) : -1;
+      // document equality as the column interval of this row's run when the ids never decrease
+      const bool runs = a.rule.any_doc && ig >= 0 && ig < a.rule.doc_len && doc_runs_usable(a.rule, bm);
+      int64_t run_lo = 0, run_hi = 0;
+      if (runs) doc_run_of(a.rule, bm, ig, run_lo, run_hi);
       const float sl2 = a.scale * kLog2e;
       float slope2 = 0.f;
       if (SK == SK_ALIBI || SK == SK_GENERIC) slope2 = a.score.alibi ? __ldg(a.score.alibi + TT.h) * kLog2e : 0.f;
@@ -460,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           Bits128 bits = {{0u, 0u, 0u, 0u}};
           if (q_row < a.q_len && w > 0) {
             bits = rule_row_bits(a.rule, ig, jh, w, doc_i, [&](int dq) {
+              if (runs) return range_bits(clamp_rel(run_lo - jh, w), clamp_rel(run_hi - jh, w));
               return doc_bits<2>(w, dq, [&](int cc) { return doc_at(a.rule, bm, jh + cc); });
             });
           }

@@ -61,6 +61,33 @@ __device__ __forceinline__ ScanOut block_scan2(int a, int b, int* s_tmp /* [8] *
   return r;
 }
 
+// Document-id runs, one thread per position (grid.y = batch row). Where the ids never decrease, the
+// run of equal ids around position t is [first position with id >= d[t], first with id > d[t]) of the
+// row: two binary searches. Any decrease clears the row's `sorted` flag (set beforehand); the bounds
+// of an unsorted row are then never read.
+__global__ void __launch_bounds__(256) doc_runs_kernel(DevRule R, int32_t* run, int32_t* sorted) {
+  const int b = blockIdx.y;
+  const int n = R.doc_len;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n) return;
+  const int32_t* d = R.doc_ids + (size_t)b * n;
+  const int v = __ldg(d + t);
+  if (t > 0 && __ldg(d + t - 1) > v) sorted[b] = 0;
+  int a = 0, z = t;  // lower bound of v in [0, t]
+  while (a < z) {
+    const int m = (a + z) >> 1;
+    if (__ldg(d + m) < v) a = m + 1; else z = m;
+  }
+  int c = t + 1, e = n;  // upper bound of v in [t + 1, n)
+  while (c < e) {
+    const int m = (c + e) >> 1;
+    if (__ldg(d + m) <= v) c = m + 1; else e = m;
+  }
+  int32_t* lo = run + (size_t)b * 2 * n;
+  lo[t] = a;
+  lo[n + t] = c;
+}
+
 constexpr uint8_t kUnknown = 0xFF;  // class not decided by the block-level test
 constexpr int kDocStage = 4096;     // column document ids staged in shared memory per visiting round
 
@@ -137,9 +164,26 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
   __shared__ int s_tmp[8];
   __shared__ int s_doc[kDocStage];  // column document ids of the blocks visited side by side
 
-  // document range of the query block's valid rows
+  // document range of the query block's valid rows (ids that never decrease: first and last row)
   int rdmin = INT_MAX, rdmax = INT_MIN;
-  if (R.any_doc) {
+  const bool sorted_ids = R.any_doc && doc_runs_usable(R, bm);
+  if (sorted_ids) {
+    if (i1 > i0) {
+      const int da = doc_at(R, bm, i0 + off), db = doc_at(R, bm, i1 - 1 + off);
+      rdmin = min(da, db);  // -1 (outside the id array) may sit at either end
+      rdmax = max(da, db);
+      if (da == -1 || db == -1) {  // mixed inside / outside: fall back to the full reduction
+        rdmin = INT_MAX;
+        rdmax = INT_MIN;
+        for (int64_t i = i0 + tid; i < i1; i += kThreads) {
+          const int d = doc_at(R, bm, i + off);
+          rdmin = min(rdmin, d);
+          rdmax = max(rdmax, d);
+        }
+        block_minmax(rdmin, rdmax, s_tmp);
+      }
+    }
+  } else if (R.any_doc) {
     for (int64_t i = i0 + tid; i < i1; i += kThreads) {
       const int d = doc_at(R, bm, i + off);
       rdmin = min(rdmin, d);
@@ -156,6 +200,9 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
   const bool row_in = active && i < T.q_len;
   const int64_t ig = i + off;
   const int doc_i = (R.any_doc && row_in) ? doc_at(R, bm, ig) : -1;
+  const bool runs = R.any_doc && row_in && ig >= 0 && ig < R.doc_len && doc_runs_usable(R, bm);
+  int64_t run_lo = 0, run_hi = 0;
+  if (runs) doc_run_of(R, bm, ig, run_lo, run_hi);
   const Bits128 full_bk = range_bits(0, Bk);
 
   const size_t row = ((size_t)bm * T.Hm + hm) * T.nq + r;
@@ -166,8 +213,17 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
   int run_p = 0, run_f = 0;
   for (int c0 = 0; c0 < nk; c0 += kChunk) {
     const int cn = min(kChunk, nk - c0);
-    // 1. document range of every column block of the chunk (a warp per block, coalesced)
-    if (R.any_doc) {
+    // 1. document range of every column block of the chunk: first and last id when the ids never
+    // decrease, else a warp per block (coalesced)
+    if (sorted_ids) {
+      for (int x = tid; x < cn; x += kThreads) {
+        const int64_t j0 = (int64_t)(c0 + x) * Bk;
+        const int64_t j1 = min(j0 + Bk, (int64_t)T.kv_len);
+        s_a[x] = doc_at(R, bm, j0);
+        s_b[x] = doc_at(R, bm, j1 - 1);
+      }
+      __syncthreads();
+    } else if (R.any_doc) {
       for (int x = warp; x < cn; x += kThreads / 32) {
         const int64_t j0 = (int64_t)(c0 + x) * Bk;
         const int w = (int)min((int64_t)Bk, (int64_t)T.kv_len - j0);
@@ -207,7 +263,7 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
       __syncthreads();
       // rounds of `lanes` blocks side by side; the blocks' column document ids are staged in shared
       // memory when they fit (every thread of the CTA takes part in the rounds and their barriers)
-      const bool stage = R.any_doc && lanes * Bk <= kDocStage;
+      const bool stage = R.any_doc && !doc_runs_usable(R, bm) && lanes * Bk <= kDocStage;  // uniform in the CTA
       for (int base = 0; base < cn; base += lanes) {
         bool round_has = false;  // same answer in every thread (s_cls is stable here)
         for (int l = 0; l < lanes && base + l < cn; ++l) round_has = round_has || s_cls[base + l] == kUnknown;
@@ -228,6 +284,7 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
           if (row_in) {
             const int* cdoc = s_doc + lam * Bk;
             Bits128 b = rule_row_bits(R, ig, j0, w, doc_i, [&](int d) {
+              if (runs) return range_bits(clamp_rel(run_lo - j0, w), clamp_rel(run_hi - j0, w));
               return stage ? doc_bits<4>(w, d, [&](int c) { return cdoc[c]; })
                            : doc_bits<4>(w, d, [&](int c) { return doc_at(R, bm, j0 + c); });
             });
@@ -347,7 +404,17 @@ __global__ void mask_stats_finish(MaskOut T, unsigned long long* out) {
 
 }  // namespace
 
-cudaError_t launch_mask_build(const DevRule& R, const MaskOut& T, cudaStream_t st) {
+cudaError_t launch_mask_build(const DevRule& R0, const MaskOut& T, cudaStream_t st) {
+  DevRule R = R0;
+  if (R.any_doc && T.doc_run && T.doc_sorted) {
+    cudaError_t e = cudaMemsetAsync(T.doc_sorted, 0xFF, sizeof(int32_t) * R.doc_batch, st);  // nonzero: sorted
+    if (e != cudaSuccess) return e;
+    doc_runs_kernel<<<dim3((R.doc_len + 255) / 256, R.doc_batch), 256, 0, st>>>(R, T.doc_run, T.doc_sorted);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    R.doc_run = T.doc_run;
+    R.doc_sorted = T.doc_sorted;
+  }
   dim3 g1(T.nq, T.Hm, T.Bm);
   mask_classify_kernel<<<g1, kThreads, 0, st>>>(R, T);
   cudaError_t e = cudaGetLastError();

@@ -48,7 +48,8 @@ class BlockMaskC(ctypes.Structure):
                 ("kv_num", ctypes.c_void_p), ("kv_idx", ctypes.c_void_p), ("full_kv_num", ctypes.c_void_p),
                 ("full_kv_idx", ctypes.c_void_p), ("q_num", ctypes.c_void_p), ("q_idx", ctypes.c_void_p),
                 ("full_q_num", ctypes.c_void_p), ("full_q_idx", ctypes.c_void_p),
-                ("block_class", ctypes.c_void_p), ("rule", MaskRule)]
+                ("block_class", ctypes.c_void_p), ("doc_run", ctypes.c_void_p), ("doc_sorted", ctypes.c_void_p),
+                ("rule", MaskRule)]
 
 
 _lib = None

@@ -123,6 +123,10 @@ typedef struct {
   int32_t* full_q_num;      /* [Bm,Hm,nk]    */
   int32_t* full_q_idx;      /* [Bm,Hm,nk,nq] */
   uint8_t* block_class;     /* [Bm,Hm,nq,nk]: 0 empty, 1 partial, 2 full */
+  int32_t* doc_run;         /* rules that read document ids: [doc_batch,2,doc_len], per position the first
+                               and one-past-last position of the run of equal ids around it; else NULL */
+  int32_t* doc_sorted;      /* [doc_batch]: 1 where the ids never decrease (each id is then one run, and
+                               the kernels test document equality as a column interval); else NULL */
   fa_mask_rule rule;
 } fa_block_mask;
 

@@ -83,6 +83,21 @@ def test_rule_sweep_unsorted_docs(ri, q_len, kv_len, bq, bk, ndoc):
     assert_tables_equal(t, orc.block_mask(spec, 1, 1, q_len, kv_len, bq, bk, doc_ids=doc))
 
 
+@pytest.mark.parametrize("sorted_ids", [True, False])
+def test_docs_with_rows_past_the_id_array(sorted_ids):
+    # query offsets push rows past the document-id array (their id reads as -1); some key ids are -1 too
+    B, H, q_len, kv_len = 2, 1, 24, 64
+    off = np.array([30, 50], dtype=np.int32)
+    rng = np.random.default_rng(11 + sorted_ids)
+    doc = rng.integers(-1, 3, size=(B, kv_len)).astype(np.int32)
+    if sorted_ids:
+        doc = np.sort(doc, axis=1)
+    spec = [("causal",), ("doc",), ("and",)]
+    _, t = gpu_tables(spec, B, H, q_len, kv_len, 8, 8, doc=doc, q_off=off, bdep=True)
+    assert_tables_equal(t, orc.block_mask(spec, B, H, q_len, kv_len, 8, 8, batch_dependent=True, q_offset=off,
+                                          doc_ids=doc))
+
+
 def test_batch_dependent_offsets_and_docs():
     B, H = 3, 2
     off = np.array([0, 17, 40], dtype=np.int32)
