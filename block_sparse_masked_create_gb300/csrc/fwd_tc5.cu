@@ -63,6 +63,7 @@ struct Tc5Cfg {
 
 struct Tc5Params {
   FwdArgs a;
+  int ahead;  // CTAs per wave: the CTA this many ids later runs next on the SM this one frees
 };
 
 // byte offset of 16-byte chunk c16 of row `row` in a [128][D] tile stored as D/64 sub-tiles [128][64]
@@ -97,6 +98,23 @@ __device__ __forceinline__ Tile make_tile(const FwdArgs& a, int b, int h, int r)
   return T;
 }
 
+// Work item p -> (batch b, head pair hp, query block r). The (b, hp) pairs are taken in groups of
+// kGroupPairs; within a group the query blocks go from the last to the first (heaviest first for causal
+// masks) with the group's pairs side by side, so the CTAs resident at any time share the K / V of a few
+// heads in L2 instead of streaming every head's K / V from DRAM once per query block.
+__device__ __forceinline__ void work_item(const FwdArgs& a, int p, int& b, int& hp, int& r) {
+  const int HP = (a.Hq + 1) / 2;
+  const int nq = a.mask.nq;
+  const int NP = a.B * HP;
+  const int GS = NP < kGroupPairs ? NP : kGroupPairs;
+  const int g = p / (GS * nq), g0 = g * GS, gs = min(GS, NP - g0);
+  const int rem = p - g * GS * nq;
+  const int pair = g0 + rem % gs;
+  hp = pair % HP;
+  b = pair / HP;
+  r = nq - 1 - rem / gs;
+}
+
 template <int D, int SK>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc5_kernel(const __grid_constant__ Tc5Params P, const __grid_constant__ CUtensorMap tmQ,
@@ -129,20 +147,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  // ---- work item: (query block r, batch b, head pair hp). The (b, hp) pairs are taken in groups of
-  // kGroupPairs; within a group the query blocks go from the last to the first (heaviest first for causal
-  // masks) with the group's pairs side by side, so the CTAs resident at any time share the K / V of a
-  // few heads in L2 instead of streaming every head's K / V from DRAM once per query block.
-  const int HP = (a.Hq + 1) / 2;
+  // ---- work item: (query block r, batch b, head pair hp)
   const DevMask& M = a.mask;
-  const int NP = a.B * HP;
-  const int GS = NP < kGroupPairs ? NP : kGroupPairs;
-  const int g = blockIdx.x / (GS * M.nq), g0 = g * GS, gs = min(GS, NP - g0);
-  const int rem = blockIdx.x - g * GS * M.nq;
-  const int pair = g0 + rem % gs;
-  const int hp = pair % HP;
-  const int b = pair / HP;
-  const int r = M.nq - 1 - rem / gs;
+  int b, hp, r;
+  work_item(a, blockIdx.x, b, hp, r);
   const Tile T0 = make_tile(a, b, 2 * hp, r);
   const Tile T1 = make_tile(a, b, 2 * hp + 1, r);
   // sibling heads of one KV head with the same mask row share K / V loads
@@ -210,6 +218,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int x = 0; x < D / 64; ++x) tma_load_3d_elect(sQ1 + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T1.h, &bar_q[1]);
     }
+    // the Q tiles of the CTA that will take this SM after the next wave go to L2 now, so its start does
+    // not wait on DRAM
+    if (P.ahead > 0 && blockIdx.x + P.ahead < gridDim.x && lane == 0) {
+      int bn, hpn, rn;
+      work_item(a, blockIdx.x + P.ahead, bn, hpn, rn);
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const Tile Tn = make_tile(a, bn, 2 * hpn + tt, rn);
+        if (Tn.n == 0) continue;
+#pragma unroll
+        for (int x = 0; x < D / 64; ++x) tma_prefetch_l2_3d(&tmQ, x * 64, rn * 128, bn * a.Hq + Tn.h);
+      }
+    }
+    __syncwarp();
     int issued = 0;
     bool ok = true;
     auto load = [&](const Tile& T, bool is_v, int j) -> bool {
@@ -553,12 +575,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool empty = m_ref == -INFINITY;
       const float inv = empty ? 0.f : 1.f / lt;
       if (ok && h == 0 && q_row < a.q_len) Lg[q_row] = empty ? -INFINITY : (m_ref + __log2f(let)) * kLn2;
-      // staging in this tile's Q buffer (D/64 sub-buffers of 16 KB; free: every Q K^T of the tile has
-      // completed). bf16: one round of D/64 boxes [128][64], each half filling its columns. fp32: two
-      // rounds of boxes [128][32] (128-byte rows); with D = 128 half h fills sub-buffer h with its
-      // columns 32 rd.. each round, with D = 64 half rd fills the only sub-buffer in round rd.
-      const int rounds = a.out_f32 ? 2 : 1;
       const bool issuer = h == 0 && (warp & 3) == 0 && lane == 0;
+      // fp32 O (two slots' worth) is staged in the K / V ring when both tiles visit the same number of
+      // blocks (or one visits none): then, once this tile's last product completed, every ring slot but
+      // the one of the CTA's last load has been consumed, in both load orders. Tile t takes the slots of
+      // the loads 2 + 2t and 3 + 2t from the end (distinct, the ring has at least five slots); boxes
+      // [128][32] (128-byte rows, 128-byte swizzle), half h filling its D/64 boxes.
+      const int n_loads = shared_kv ? 2 * T0.n : 2 * (T0.n + T1.n);
+      const bool ring_stage = a.out_f32 && (T0.n == T1.n || T0.n == 0 || T1.n == 0);
+      auto box_smem = [&](int kb) -> uint8_t* {
+        int sl = (n_loads - (2 + 2 * t + (kb * 16384) / C::kSlotBytes)) % NST;
+        sl = sl < 0 ? sl + NST : sl;
+        return sRing + sl * C::kSlotBytes + (kb * 16384) % C::kSlotBytes;
+      };
+      if (ring_stage) {
+        if (ok) {
+#pragma unroll
+          for (int kb = h * (D / 64); kb < (h + 1) * (D / 64); ++kb) {
+            uint8_t* const stg = box_smem(kb);
+            uint32_t o[32];
+            tc5_ld32(tO + kb * 32, o);
+            tc5_wait_ld();
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              float4 v = make_float4(__uint_as_float(o[4 * q4 + 0]) * inv, __uint_as_float(o[4 * q4 + 1]) * inv,
+                                     __uint_as_float(o[4 * q4 + 2]) * inv, __uint_as_float(o[4 * q4 + 3]) * inv);
+              *reinterpret_cast<float4*>(stg + row * 128 + ((q4 ^ (row & 7)) << 4)) = v;
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1 + t, 256);
+        if (!*wc.abort && issuer) {
+#pragma unroll
+          for (int kb = 0; kb < D / 32; ++kb) tma_store_3d(&tmO, box_smem(kb), kb * 32, r * 128, b * a.Hq + TT.h);
+          bulk_commit_group();
+        }
+      }
+      // otherwise staging in this tile's Q buffer (D/64 sub-buffers of 16 KB; free: every Q K^T of the
+      // tile has completed). bf16: one round of D/64 boxes [128][64], each half filling its columns. fp32:
+      // two rounds of boxes [128][32]; with D = 128 half h fills sub-buffer h with its columns 32 rd..
+      // each round, with D = 64 half rd fills the only sub-buffer in round rd.
+      const int rounds = ring_stage ? 0 : (a.out_f32 ? 2 : 1);
       for (int rd = 0; rd < rounds; ++rd) {
         if (rd > 0) {
           if (issuer) bulk_wait_group_read0();  // the previous round's boxes have left shared memory
@@ -644,6 +702,10 @@ int launch_k(const FwdArgs& a, cudaStream_t st) {
   Tc5Params p;
   std::memset(&p, 0, sizeof(p));
   p.a = a;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  p.ahead = sms;
   const int n_pairs = a.B * a.mask.nq * ((a.Hq + 1) / 2);
   auto kern = fwd_tc5_kernel<D, SK>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
