@@ -32,11 +32,17 @@
 namespace fa {
 namespace {
 
-// 16 softmax warps (2 warpgroups per tile), the TMA producer and the MMA issuer. Five warps share an
-// SM sub-partition, which caps a thread at 96 registers; the softmax fits (it holds 64 scores).
-constexpr int kThreads = 576;
-constexpr int kLoadWarp = 16;
-constexpr int kMmaWarp = 17;
+// NT query tiles per CTA (2: one CTA per SM; 1: two CTAs per SM, whose start-up and epilogue then
+// overlap each other's work). Per tile 8 softmax warps (2 warpgroups), then the TMA producer and the MMA
+// issuer. At most five warps share an SM sub-partition either way, which caps a thread at 96 registers;
+// the softmax fits (it holds 64 scores).
+template <int NT>
+struct Roles {
+  static constexpr int kLoadWarp = 8 * NT;
+  static constexpr int kMmaWarp = 8 * NT + 1;
+  static constexpr int kThreads = (8 * NT + 2) * 32;
+  static constexpr int kCtasPerSm = NT == 2 ? 1 : 2;
+};
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 2^8
@@ -44,17 +50,18 @@ constexpr int kGroupPairs = 8;             // (batch, head pair) units sharing t
 
 enum ScoreKind { SK_NONE = 0, SK_ALIBI = 1, SK_SOFTCAP = 2, SK_GENERIC = 3 };
 
-template <int D>
+template <int D, int NT>
 struct Tc5Cfg {
   static constexpr int kQBytes = 128 * D * 2;      // one Q tile (also the O staging tile)
   static constexpr int kSlotBytes = 128 * D * 2;   // one K or V tile
-  static constexpr int kStages = D == 128 ? 5 : 12;
-  static constexpr int kOffRing = 2 * kQBytes;
+  // K / V ring: what is left of the shared memory of an SM (two CTAs: half of it each)
+  static constexpr int kStages = NT == 2 ? (D == 128 ? 5 : 12) : (D == 128 ? 2 : 5);
+  static constexpr int kOffRing = NT * kQBytes;
   static constexpr int kOffRed = kOffRing + kStages * kSlotBytes;  // float [tile][half][row] exchange
   static constexpr int kOffBar = kOffRed + 2 * 2 * 128 * 4;        // mbarriers, TMEM address, abort flag
   static constexpr int kSmem = kOffBar + 512;
-  static_assert(kSmem <= 227 * 1024, "shared memory budget");
-  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kSmem * (NT == 2 ? 1 : 2) + (NT == 2 ? 0 : 1024) <= 227 * 1024, "shared memory budget");
+  static constexpr uint32_t kTmemCols = 256 * NT;
   // tensor-memory columns: S_t at [256 t, 256 t + 128), with P_t (bf16 pairs) over columns [0, 32) and
   // [64, 96) of it (keys 0..63 and 64..127); O_t at [256 t + 128, 256 t + 128 + D)
   __device__ static constexpr uint32_t col_s(int t) { return (uint32_t)t * 256u; }
@@ -98,12 +105,13 @@ __device__ __forceinline__ Tile make_tile(const FwdArgs& a, int b, int h, int r)
   return T;
 }
 
-// Work item p -> (batch b, head pair hp, query block r). The (b, hp) pairs are taken in groups of
+// Work item p -> (batch b, head group hp of NT heads, query block r). The (b, hp) units are taken in groups of
 // kGroupPairs; within a group the query blocks go from the last to the first (heaviest first for causal
 // masks) with the group's pairs side by side, so the CTAs resident at any time share the K / V of a few
 // heads in L2 instead of streaming every head's K / V from DRAM once per query block.
+template <int NT>
 __device__ __forceinline__ void work_item(const FwdArgs& a, int p, int& b, int& hp, int& r) {
-  const int HP = (a.Hq + 1) / 2;
+  const int HP = (a.Hq + NT - 1) / NT;
   const int nq = a.mask.nq;
   const int NP = a.B * HP;
   const int GS = NP < kGroupPairs ? NP : kGroupPairs;
@@ -115,12 +123,14 @@ __device__ __forceinline__ void work_item(const FwdArgs& a, int p, int& b, int& 
   r = nq - 1 - rem / gs;
 }
 
-template <int D, int SK>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int SK, int NT>
+__global__ void __launch_bounds__(Roles<NT>::kThreads, Roles<NT>::kCtasPerSm)
     fwd_tc5_kernel(const __grid_constant__ Tc5Params P, const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmO) {
-  using C = Tc5Cfg<D>;
+  using C = Tc5Cfg<D, NT>;
+  constexpr int kLoadWarp = Roles<NT>::kLoadWarp;
+  constexpr int kMmaWarp = Roles<NT>::kMmaWarp;
   constexpr int NST = C::kStages;
   const FwdArgs& a = P.a;
   // All shared state is dynamic (no static __shared__), so the buffer starts at the CTA's shared
@@ -150,9 +160,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- work item: (query block r, batch b, head pair hp)
   const DevMask& M = a.mask;
   int b, hp, r;
-  work_item(a, blockIdx.x, b, hp, r);
-  const Tile T0 = make_tile(a, b, 2 * hp, r);
-  const Tile T1 = make_tile(a, b, 2 * hp + 1, r);
+  work_item<NT>(a, blockIdx.x, b, hp, r);
+  const Tile T0 = make_tile(a, b, NT * hp, r);
+  const Tile T1 = make_tile(a, b, NT == 2 ? 2 * hp + 1 : a.Hq, r);  // NT = 1: no second tile
   // sibling heads of one KV head with the same mask row share K / V loads
   const bool shared_kv = T1.valid && T0.hk == T1.hk && T0.n > 0 && M.Hm == 1;
   const int nmax = max(T0.n, T1.n);
@@ -222,10 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // not wait on DRAM
     if (P.ahead > 0 && blockIdx.x + P.ahead < gridDim.x && lane == 0) {
       int bn, hpn, rn;
-      work_item(a, blockIdx.x + P.ahead, bn, hpn, rn);
+      work_item<NT>(a, blockIdx.x + P.ahead, bn, hpn, rn);
 #pragma unroll
-      for (int tt = 0; tt < 2; ++tt) {
-        const Tile Tn = make_tile(a, bn, 2 * hpn + tt, rn);
+      for (int tt = 0; tt < NT; ++tt) {
+        const Tile Tn = make_tile(a, bn, NT * hpn + tt, rn);
         if (Tn.n == 0) continue;
 #pragma unroll
         for (int x = 0; x < D / 64; ++x) tma_prefetch_l2_3d(&tmQ, x * 64, rn * 128, bn * a.Hq + Tn.h);
@@ -584,7 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_loads = shared_kv ? 2 * T0.n : 2 * (T0.n + T1.n);
       const bool ring_stage = a.out_f32 && (T0.n == T1.n || T0.n == 0 || T1.n == 0);
       auto box_smem = [&](int kb) -> uint8_t* {
-        int sl = (n_loads - (2 + 2 * t + (kb * 16384) / C::kSlotBytes)) % NST;
+        // one tile per CTA: its last product is the CTA's last MMA, so every slot is free
+        int sl = (n_loads - ((NT == 2 ? 2 + 2 * t : 1) + (kb * 16384) / C::kSlotBytes)) % NST;
         sl = sl < 0 ? sl + NST : sl;
         return sRing + sl * C::kSlotBytes + (kb * 16384) % C::kSlotBytes;
       };
@@ -680,9 +691,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int SK>
+template <int D, int SK, int NT>
 int launch_k(const FwdArgs& a, cudaStream_t st) {
-  using C = Tc5Cfg<D>;
+  using C = Tc5Cfg<D, NT>;
   CUtensorMap tq, tk, tv, to;
   const uint64_t dq[3] = {(uint64_t)D, (uint64_t)a.q_len, (uint64_t)a.B * a.Hq};
   const uint64_t dk[3] = {(uint64_t)D, (uint64_t)a.kv_len, (uint64_t)a.B * a.Hkv};
@@ -705,22 +716,45 @@ int launch_k(const FwdArgs& a, cudaStream_t st) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return FA_ERR_CUDA;
-  p.ahead = sms;
-  const int n_pairs = a.B * a.mask.nq * ((a.Hq + 1) / 2);
-  auto kern = fwd_tc5_kernel<D, SK>;
+  p.ahead = sms * Roles<NT>::kCtasPerSm;
+  const int n_items = a.B * a.mask.nq * ((a.Hq + NT - 1) / NT);
+  auto kern = fwd_tc5_kernel<D, SK, NT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
     return FA_ERR_CUDA;
-  kern<<<n_pairs, kThreads, C::kSmem, st>>>(p, tq, tk, tv, to);
+  kern<<<n_items, Roles<NT>::kThreads, C::kSmem, st>>>(p, tq, tk, tv, to);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int D, int NT>
+int launch_sk(const FwdArgs& a, cudaStream_t st) {
+  const bool al = a.score.alibi != nullptr, rel = a.score.rel != nullptr, cap = a.score.softcap > 0.f;
+  if (!al && !rel && !cap) return launch_k<D, SK_NONE, NT>(a, st);
+  if (al && !rel && !cap) return launch_k<D, SK_ALIBI, NT>(a, st);
+  if (!al && !rel && cap) return launch_k<D, SK_SOFTCAP, NT>(a, st);
+  return launch_k<D, SK_GENERIC, NT>(a, st);
+}
+
+// Tiles per CTA. Two tiles of sibling heads share one CTA (and, for grouped query heads, every K / V
+// load); one tile per CTA lets two CTAs share an SM, which pays where rows are short and a CTA's
+// start-up and epilogue are a large part of its life.
+// Measured: sliding windows of up to 2048 keys (at most 17 blocks a row) with one KV head per query head
+// gain about 5 % with one tile per CTA; long rows lose about 8 % (the ring is then two slots deep), and
+// grouped query heads would lose their shared K / V loads.
+int tiles_per_cta(const FwdArgs& a) {
+#ifdef FA_TC5_TILES
+  (void)a;
+  return FA_TC5_TILES;
+#else
+  bool windowed = a.rule.n_terms > 0;
+  for (int i = 0; i < a.rule.n_terms; ++i)
+    if (a.rule.t[i].win == INT64_MAX || a.rule.t[i].win > 2048) windowed = false;
+  return (windowed && a.Hq == a.Hkv) ? 1 : 2;
+#endif
 }
 
 template <int D>
 int launch_d(const FwdArgs& a, cudaStream_t st) {
-  const bool al = a.score.alibi != nullptr, rel = a.score.rel != nullptr, cap = a.score.softcap > 0.f;
-  if (!al && !rel && !cap) return launch_k<D, SK_NONE>(a, st);
-  if (al && !rel && !cap) return launch_k<D, SK_ALIBI>(a, st);
-  if (!al && !rel && cap) return launch_k<D, SK_SOFTCAP>(a, st);
-  return launch_k<D, SK_GENERIC>(a, st);
+  return tiles_per_cta(a) == 1 ? launch_sk<D, 1>(a, st) : launch_sk<D, 2>(a, st);
 }
 
 }  // namespace
