@@ -171,31 +171,63 @@ __global__ void __launch_bounds__(Roles<NT>::kThreads, Roles<NT>::kCtasPerSm)
   uint8_t* sQ1 = smem + C::kQBytes;
   uint8_t* sRing = smem + C::kOffRing;
 
-  if (tid == 0) {
-    s_abort = 0;
+  // ring loads issued so far (producer warp); the ring fill starts before the CTA-wide barrier below
+  int issued = 0;
+  auto load_slot = [&](const Tile& T, bool is_v, int j) {  // into the next slot, which must be free
+    const int s = issued % NST;
+    const int c = T.col(j);
+    uint8_t* dst = sRing + s * C::kSlotBytes;
+    mbar_arrive_expect_tx_elect(&bar_full[s], C::kSlotBytes);
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(&bar_q[t], 1);
-      mbar_init(&bar_s[t], 1);
-      mbar_init(&bar_p[t], 256);
-      mbar_init(&bar_o[t], 1);
+    for (int x = 0; x < D / 64; ++x)
+      tma_load_3d_elect(dst + x * 16384, is_v ? &tmV : &tmK, x * 64, c * 128, b * a.Hkv + T.hk, &bar_full[s]);
+    ++issued;
+  };
+  if (warp == kLoadWarp) {
+    // The producer sets up the barriers and sends the Q tiles and the first K tiles at once (they need
+    // nothing else), while the MMA warp allocates tensor memory.
+    if (lane == 0) {
+      s_abort = 0;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        mbar_init(&bar_q[t], 1);
+        mbar_init(&bar_s[t], 1);
+        mbar_init(&bar_p[t], 256);
+        mbar_init(&bar_o[t], 1);
+      }
+      for (int s = 0; s < NST; ++s) {
+        mbar_init(&bar_full[s], 1);
+        mbar_init(&bar_empty[s], 1);
+      }
+      mbar_init(&bar_drain, 1);
+      fence_mbar_init();
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmO);
     }
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1);
+    __syncwarp();
+    if (T0.n > 0) {
+      mbar_arrive_expect_tx_elect(&bar_q[0], C::kQBytes);
+#pragma unroll
+      for (int x = 0; x < D / 64; ++x) tma_load_3d_elect(sQ0 + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T0.h, &bar_q[0]);
     }
-    mbar_init(&bar_drain, 1);
-    fence_mbar_init();
+    if (T1.n > 0) {
+      mbar_arrive_expect_tx_elect(&bar_q[1], C::kQBytes);
+#pragma unroll
+      for (int x = 0; x < D / 64; ++x) tma_load_3d_elect(sQ1 + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T1.h, &bar_q[1]);
+    }
+    // first K tiles in load order (K(0) shared, or K0(0) K1(0)); at most two, the ring has more slots
+    if (shared_kv) {
+      load_slot(T0, false, 0);
+    } else {
+      if (T0.n > 0) load_slot(T0, false, 0);
+      if (T1.n > 0) load_slot(T1, false, 0);
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&s_tmem, C::kTmemCols);
     tmem_relinquish();
-  }
-  if (warp == kLoadWarp && lane == 0) {
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmO);
   }
   tc5_fence_before();
   __syncthreads();
@@ -218,16 +250,6 @@ __global__ void __launch_bounds__(Roles<NT>::kThreads, Roles<NT>::kCtasPerSm)
       atomicAdd(cnt + 3, (unsigned long long)(shared_kv ? vis : 2 * vis));
     }
     __syncwarp();
-    if (T0.n > 0) {
-      mbar_arrive_expect_tx_elect(&bar_q[0], C::kQBytes);
-#pragma unroll
-      for (int x = 0; x < D / 64; ++x) tma_load_3d_elect(sQ0 + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T0.h, &bar_q[0]);
-    }
-    if (T1.n > 0) {
-      mbar_arrive_expect_tx_elect(&bar_q[1], C::kQBytes);
-#pragma unroll
-      for (int x = 0; x < D / 64; ++x) tma_load_3d_elect(sQ1 + x * 16384, &tmQ, x * 64, r * 128, b * a.Hq + T1.h, &bar_q[1]);
-    }
     // the Q tiles of the CTA that will take this SM after the next wave go to L2 now, so its start does
     // not wait on DRAM
     if (P.ahead > 0 && blockIdx.x + P.ahead < gridDim.x && lane == 0) {
@@ -242,31 +264,22 @@ __global__ void __launch_bounds__(Roles<NT>::kThreads, Roles<NT>::kCtasPerSm)
       }
     }
     __syncwarp();
-    int issued = 0;
     bool ok = true;
     auto load = [&](const Tile& T, bool is_v, int j) -> bool {
       const int s = issued % NST;
       if (issued >= NST &&
           !__all_sync(0xFFFFFFFFu, mbar_wait(&bar_empty[s], (uint32_t)(((issued / NST) - 1) & 1), wc)))
         return false;
-      const int c = T.col(j);
-      uint8_t* dst = sRing + s * C::kSlotBytes;
-      mbar_arrive_expect_tx_elect(&bar_full[s], C::kSlotBytes);
-#pragma unroll
-      for (int x = 0; x < D / 64; ++x)
-        tma_load_3d_elect(dst + x * 16384, is_v ? &tmV : &tmK, x * 64, c * 128, b * a.Hkv + T.hk, &bar_full[s]);
-      ++issued;
+      load_slot(T, is_v, j);
       return true;
     };
+    // K(0) / K0(0) K1(0) went out before the CTA-wide barrier
     if (shared_kv) {
-      ok = load(T0, false, 0);
       for (int j = 0; j < T0.n && ok; ++j) {
         ok = load(T0, true, j);
         if (ok && j + 1 < T0.n) ok = load(T0, false, j + 1);
       }
     } else {
-      if (T0.n > 0) ok = load(T0, false, 0);
-      if (ok && T1.n > 0) ok = load(T1, false, 0);
       for (int j = 0; j < nmax && ok; ++j) {
         if (j < T0.n) {
           ok = load(T0, true, j);
