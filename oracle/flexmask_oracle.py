@@ -256,6 +256,49 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, rule, scale: Optional
     return o, lse
 
 
+def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, do: np.ndarray, rule,
+                       scale: Optional[float] = None, score: Optional[dict] = None,
+                       q_offset: Optional[np.ndarray] = None, doc_ids: Optional[np.ndarray] = None):
+    """Gradients of the masked attention output O with respect to q, k, v for an upstream gradient dO
+    ([FA] backward questions; [FX] 4.2): with s the scaled score, s' = score_mod(s) and P = softmax(s')
+    over the allowed pairs,
+        dV = P^T dO,  dP = dO V^T,  D_i = sum_d dO_id O_id,  dS' = P * (dP - D),
+        dS = dS' * ds'/ds  (1 - (s'/c)^2 under the soft-cap c; biases do not depend on q or k),
+        dQ = scale dS K,  dK = scale dS^T Q,
+    summed over the query heads that share a KV head. Masked pairs and empty rows carry no gradient.
+    q [B,Hq,Q_LEN,d], k/v [B,Hkv,KV_LEN,d], do like q (fp64). Returns dq, dk, dv (fp64)."""
+    B, Hq, q_len, d = q.shape
+    Hkv, kv_len = k.shape[1], k.shape[2]
+    g = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = np.zeros_like(q, dtype=np.float64)
+    dk = np.zeros_like(k, dtype=np.float64)
+    dv = np.zeros_like(v, dtype=np.float64)
+    rows = np.arange(q_len, dtype=np.int64)
+    j = np.arange(kv_len, dtype=np.int64)
+    c = float((score or {}).get("softcap", 0.0) or 0.0)
+    for b in range(B):
+        off = 0 if q_offset is None else int(q_offset[b])
+        a = dense_allowed(rule, b, rows, q_len, kv_len, off, doc_ids)
+        for h in range(Hq):
+            hk = h // g
+            s = scale * (q[b, h] @ k[b, hk].T)
+            sm = score_mod(s, h, rows[:, None] + off, j[None, :], score, kv_len)
+            o, _, p = attention_rows(q[b, h], k[b, hk], v[b, hk], rule, rows, b, h, q_len, kv_len, scale,
+                                     score, off, doc_ids, return_p=True)
+            dv[b, hk] += p.T @ do[b, h]
+            dp = do[b, h] @ v[b, hk].T
+            delta = np.sum(do[b, h] * o, axis=1)
+            ds = p * (dp - delta[:, None])
+            if c > 0.0:
+                ds = ds * (1.0 - (sm / c) ** 2)
+            ds = np.where(a, ds, 0.0)
+            dq[b, h] = scale * (ds @ k[b, hk])
+            dk[b, hk] += scale * (ds.T @ q[b, h])
+    return dq, dk, dv
+
+
 def merge_partials(m: np.ndarray, l: np.ndarray, u: np.ndarray):
     """Merge split-softmax states ([K5] section 3): m = max_s m_s, l = sum_s e^(m_s - m) l_s,
     u = sum_s e^(m_s - m) u_s, O = u / l, LSE = m + ln l. Axis 0 indexes the splits; an empty split has

@@ -442,3 +442,79 @@ def test_planted_mistakes_fail_pins(golden_dir, monkeypatch):
     monkeypatch.setattr(orc, "attention_rows", unscaled)
     with pytest.raises(AssertionError):
         test_matches_torch_sdpa_fp64(True)
+
+
+# ------------------------------------------------------------------ backward
+def _finite_difference_check(rule, score, B=1, Hq=2, Hkv=1, N=11, d=6, doc=None, seed=0, samples=6):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, Hq, N, d))
+    k = rng.standard_normal((B, Hkv, N, d))
+    v = rng.standard_normal((B, Hkv, N, d))
+    do = rng.standard_normal((B, Hq, N, d))
+    dq, dk, dv = orc.attention_backward(q, k, v, do, rule, None, score, doc_ids=doc)
+
+    def loss(q_, k_, v_):
+        o, _ = orc.attention(q_, k_, v_, rule, None, score, doc_ids=doc)
+        return float(np.sum(o * do))
+
+    eps = 1e-6
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for _ in range(samples):
+            idx = tuple(int(rng.integers(0, n)) for n in x.shape)
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - grad[idx]) < 1e-6 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+@pytest.mark.parametrize("case", ["causal_window_softcap_alibi", "doc_prefix", "dense_gqa", "empty_rows"])
+def test_backward_matches_finite_differences(case):
+    # central differences of L = sum(O * dO) (brute force, independent of the gradient formulas)
+    if case == "causal_window_softcap_alibi":
+        _finite_difference_check([("causal",), ("window", 5), ("and",)], {"softcap": 3.0, "alibi_slopes": [0.5, 0.25]})
+    elif case == "doc_prefix":
+        doc = np.array([[0, 0, 0, 1, 1, 1, 1, 2, 2, 2, 2]], dtype=np.int32)
+        _finite_difference_check([("causal",), ("prefix", 2), ("or",), ("doc",), ("and",)], None, doc=doc, seed=1)
+    elif case == "dense_gqa":
+        _finite_difference_check([("true",)], None, Hq=4, Hkv=2, seed=2)
+    else:  # rows that see nothing carry no gradient, and nothing flows to the keys they cannot see
+        _finite_difference_check([("prefix", 0)], None, seed=3)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_torch_autograd(causal):
+    # the same gradients from torch's autograd of torch.softmax on fp64 tensors (a library routine)
+    rng = np.random.default_rng(7 + causal)
+    B, Hq, Hkv, N, d = 2, 4, 2, 9, 8
+    q = rng.standard_normal((B, Hq, N, d))
+    k = rng.standard_normal((B, Hkv, N, d))
+    v = rng.standard_normal((B, Hkv, N, d))
+    do = rng.standard_normal((B, Hq, N, d))
+    rule = [("causal",)] if causal else [("true",)]
+    dq, dk, dv = orc.attention_backward(q, k, v, do, rule, 0.3, {"softcap": 2.5})
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    ke, ve = tk.repeat_interleave(Hq // Hkv, dim=1), tv.repeat_interleave(Hq // Hkv, dim=1)
+    s = 2.5 * torch.tanh(0.3 * (tq @ ke.transpose(-1, -2)) / 2.5)
+    if causal:
+        s = s.masked_fill(~torch.ones(N, N, dtype=torch.bool).tril(), float("-inf"))
+    o = torch.softmax(s, dim=-1) @ ve
+    gq, gk, gv = torch.autograd.grad(o, (tq, tk, tv), torch.tensor(do))
+    np.testing.assert_allclose(dq, gq.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, gk.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, gv.numpy(), atol=1e-12)
+
+
+def test_planted_backward_mistake_is_caught(monkeypatch):
+    real = orc.attention_backward
+
+    def no_cap_derivative(q, k, v, do, rule, scale=None, score=None, q_offset=None, doc_ids=None):
+        # plant: the soft-cap chain-rule factor dropped (gradient taken as if s' = s)
+        rng_q, rng_k, rng_v = real(q, k, v, do, rule, scale, None, q_offset, doc_ids)
+        return rng_q, rng_k, rng_v
+
+    monkeypatch.setattr(orc, "attention_backward", no_cap_derivative)
+    with pytest.raises(AssertionError):
+        test_backward_matches_torch_autograd(False)
