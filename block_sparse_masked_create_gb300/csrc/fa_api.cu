@@ -122,6 +122,10 @@ static DevMask dev_mask(const fa_block_mask* m) {
   d.kv_idx = m->kv_idx;
   d.full_kv_num = m->full_kv_num;
   d.full_kv_idx = m->full_kv_idx;
+  d.q_num = m->q_num;
+  d.q_idx = m->q_idx;
+  d.full_q_num = m->full_q_num;
+  d.full_q_idx = m->full_q_idx;
   return d;
 }
 
@@ -275,6 +279,49 @@ static int forward_impl(bool force_mma, const void* q, const void* k, const void
   return launch_fwd_mma(a, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+static int backward_impl(const void* q, const void* k, const void* v, const void* out, int32_t out_dtype,
+                         const void* dout, const float* lse, const fa_block_mask* bm, const fa_score_rule* score,
+                         float scale, float* dq, float* dk, float* dv, float* delta, int32_t B, int32_t Hq,
+                         int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d, int32_t* dev_status,
+                         fa_stream_t stream) {
+  if (!dout || !dq || !dk || !dv || !delta) return FA_ERR_INVALID_ARG;
+  int s = check_forward(q, k, v, bm, const_cast<void*>(out), const_cast<float*>(lse), B, Hq, Hkv, Q_LEN, KV_LEN, d);
+  if (s != FA_OK) return s;
+  if (out_dtype != FA_OUT_BF16 && out_dtype != FA_OUT_F32) return FA_ERR_INVALID_ARG;
+  if ((bm->bq != 64 && bm->bq != 128) || (bm->bk != 64 && bm->bk != 128)) return FA_ERR_UNSUPPORTED;
+  if (!bm->q_num || !bm->q_idx || !bm->full_q_num || !bm->full_q_idx) return FA_ERR_INVALID_ARG;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return FA_ERR_INVALID_ARG;
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  s = compile_rule(&bm->rule, &a.rule);
+  if (s != FA_OK) return s;
+  a.rule.doc_run = bm->doc_run;
+  a.rule.doc_sorted = bm->doc_sorted;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.out_f32 = out_dtype == FA_OUT_F32;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.delta = delta;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.q_len = Q_LEN;
+  a.kv_len = KV_LEN;
+  a.d = d;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt((float)d);
+  a.score = make_score(score, KV_LEN);
+  a.mask = dev_mask(bm);
+  a.status = dev_status;
+  if ((long long)B * Hq > 65535LL * 65535LL || Hq > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
+  return launch_backward(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -384,6 +431,15 @@ fa_status fa_flex_forward_mma(const void* q, const void* k, const void* v, const
                               int32_t d, int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream) {
   return (fa_status)forward_impl(true, q, k, v, block_mask, score_rule, scale, out, out_dtype, lse, B, Hq, Hkv, Q_LEN,
                                  KV_LEN, d, dev_status, dev_counters, stream);
+}
+
+fa_status fa_flex_backward(const void* q, const void* k, const void* v, const void* out, int32_t out_dtype,
+                           const void* dout, const float* lse, const fa_block_mask* block_mask,
+                           const fa_score_rule* score_rule, float scale, float* dq, float* dk, float* dv,
+                           float* delta, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d,
+                           int32_t* dev_status, fa_stream_t stream) {
+  return (fa_status)backward_impl(q, k, v, out, out_dtype, dout, lse, block_mask, score_rule, scale, dq, dk, dv, delta,
+                                  B, Hq, Hkv, Q_LEN, KV_LEN, d, dev_status, stream);
 }
 
 size_t fa_decode_workspace_bytes(int32_t Bz, int32_t Hq, int32_t d, int32_t max_pages, int32_t page) {

@@ -72,6 +72,20 @@ __device__ __forceinline__ int doc_at(const DevRule& R, int b, int64_t pos) {
   return (pos >= 0 && pos < R.doc_len) ? __ldg(row + pos) : -1;
 }
 
+// Whether the rule allows the pair (query position ig, key position j), one pair at a time; doc_i /
+// doc_j are the two positions' document ids (read only by document terms). Same terms as rule_row_bits.
+__device__ __forceinline__ bool rule_allows(const DevRule& R, int64_t ig, int64_t j, int doc_i, int doc_j) {
+  for (int t = 0; t < R.n_terms; ++t) {
+    const DevTerm T = R.t[t];
+    if (T.causal && j > ig) continue;
+    if (T.win != INT64_MAX && ig - j >= T.win) continue;
+    if (T.pre != INT64_MAX && j >= T.pre) continue;
+    if (T.doc && doc_i != doc_j) continue;
+    return true;
+  }
+  return false;
+}
+
 // Whether document equality of batch row b can be read from run bounds (ids non-decreasing).
 __device__ __forceinline__ bool doc_runs_usable(const DevRule& R, int b) {
   return R.doc_run != nullptr && __ldg(R.doc_sorted + (R.doc_batch > 1 ? b : 0)) != 0;
@@ -512,9 +526,7 @@ struct DevScore {
   int32_t kv_len;
 };
 
-// c * tanh(x / c) with tanh(y) = sign(y) * (1 - 2 / (e^{2|y|} + 1)) (an exact identity). The absolute
-// error of tanh is a few ulp of 1 (ex2.approx has relative error ~2^-22, the division ~2 ulp), so the
-// absolute error of the capped score is a few ulp of c.
+// 2^x on the special-function unit (flushes subnormal results to zero)
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

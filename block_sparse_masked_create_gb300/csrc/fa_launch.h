@@ -16,6 +16,10 @@ struct DevMask {
   const int32_t* kv_idx;
   const int32_t* full_kv_num;
   const int32_t* full_kv_idx;
+  const int32_t* q_num;        // query-side transpose (the backward's key-block columns)
+  const int32_t* q_idx;
+  const int32_t* full_q_num;
+  const int32_t* full_q_idx;
 };
 
 struct MaskOut {
@@ -82,6 +86,28 @@ struct DecArgs {
 };
 
 int launch_decode(const DecArgs& a, cudaStream_t st);
+
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* out;     // the forward's O
+  int32_t out_f32;     // 1: O is fp32, 0: bf16
+  const void* dout;    // bf16, layout of q
+  const float* lse;    // the forward's LSE (natural log)
+  float* dq;           // fp32, layout of q
+  float* dk;           // fp32, layout of k
+  float* dv;           // fp32, layout of v
+  float* delta;        // [B, Hq, q_len] scratch: rowsum(dO * O)
+  int32_t B, Hq, Hkv, q_len, kv_len, d;
+  float scale;
+  DevRule rule;
+  DevScore score;
+  DevMask mask;
+  int32_t* status;
+};
+
+cudaError_t launch_backward(const BwdArgs& a, cudaStream_t st);
 
 cudaError_t launch_debug_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t st);
 

@@ -82,6 +82,9 @@ def load() -> ctypes.CDLL:
     lib.fa_flex_forward.argtypes = fwd_args
     lib.fa_flex_forward_mma.restype = ctypes.c_int
     lib.fa_flex_forward_mma.argtypes = fwd_args
+    lib.fa_flex_backward.restype = ctypes.c_int
+    lib.fa_flex_backward.argtypes = [vp, vp, vp, vp, i32, vp, vp, P(BlockMaskC), P(ScoreRule), f32, vp, vp, vp, vp,
+                                     i32, i32, i32, i32, i32, i32, vp, vp]
     lib.fa_decode_workspace_bytes.restype = sz
     lib.fa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.fa_flex_decode.restype = ctypes.c_int
@@ -160,6 +163,7 @@ def make_mask_rule(spec: Sequence[tuple], doc_ids: Optional[torch.Tensor] = None
         batch_dependent = q_offset is not None or (doc_ids is not None and doc_ids.shape[0] > 1)
     r.batch_dependent = int(bool(batch_dependent))
     r.head_dependent = int(bool(head_dependent))
+    r._tensors = (doc_ids, q_offset)  # the raw pointers above stay valid while the rule lives
     return r
 
 
@@ -172,6 +176,7 @@ def make_score_rule(alibi_slopes: Optional[torch.Tensor] = None, rel_bias: Optio
     s.alibi_slopes = None if alibi_slopes is None else alibi_slopes.data_ptr()
     s.rel_bias = None if rel_bias is None else rel_bias.data_ptr()
     s.softcap = float(softcap or 0.0)
+    s._tensors = (alibi_slopes, rel_bias)  # the raw pointers above stay valid while the rule lives
     return s
 
 
@@ -275,6 +280,30 @@ def flex_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: 
               float(scale) if scale else 0.0, _ptr(out), _out_code(out), _ptr(lse), B, Hq, Hkv, Q_LEN, KV_LEN, d,
               _ptr(status), _ptr(counters), _stream(q.device)), "fa_flex_forward")
     return out, lse
+
+
+def flex_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+                  dout: torch.Tensor, block_mask: BlockMask, score: Optional[ScoreRule] = None,
+                  scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
+                  dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+                  delta: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None):
+    """fa_flex_backward: gradients (dq, dk, dv) in fp32 of fa_flex_forward's out for the upstream gradient
+    dout (bf16, layout of q); out and lse are that forward's outputs."""
+    for t in (q, k, v, dout):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q, k, v, dout must be contiguous bf16 CUDA tensors")
+    B, Hq, Q_LEN, d = q.shape
+    Hkv, KV_LEN = k.shape[1], k.shape[2]
+    dev = q.device
+    dq = torch.empty(q.shape, dtype=torch.float32, device=dev) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=torch.float32, device=dev) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=torch.float32, device=dev) if dv is None else dv
+    delta = torch.empty((B, Hq, Q_LEN), dtype=torch.float32, device=dev) if delta is None else delta
+    _check(load().fa_flex_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _out_code(out), _ptr(dout), _ptr(lse),
+                                   ctypes.byref(block_mask.c), ctypes.byref(score) if score else None,
+                                   float(scale) if scale else 0.0, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta),
+                                   B, Hq, Hkv, Q_LEN, KV_LEN, d, _ptr(status), _stream(dev)), "fa_flex_backward")
+    return dq, dk, dv
 
 
 def decode_workspace_bytes(Bz: int, Hq: int, d: int, max_pages: int, page: int) -> int:

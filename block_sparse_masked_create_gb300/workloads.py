@@ -25,7 +25,7 @@ import numpy as np
 
 from . import synth
 
-TID_Q, TID_K, TID_V, TID_DOC, TID_KVLEN, TID_PERM = 1, 2, 3, 4, 5, 6
+TID_Q, TID_K, TID_V, TID_DOC, TID_KVLEN, TID_PERM, TID_DOUT = 1, 2, 3, 4, 5, 6, 7
 
 
 def seed_for(k: int) -> int:
@@ -54,6 +54,10 @@ class Prefill:
     v_bits: Optional[np.ndarray] = None
     doc_ids: Optional[np.ndarray] = None         # int32 [1, kv_len] (or None)
     meta: dict = field(default_factory=dict)
+
+    def dout_bits(self) -> np.ndarray:
+        """Seeded upstream gradient for the backward, bf16 bits [B,Hq,q_len,d] ~ N(0,1)."""
+        return synth.normal_bf16_bits(self.seed, TID_DOUT, (self.B, self.Hq, self.q_len, self.d))
 
     def generate(self) -> "Prefill":
         self.q_bits = synth.normal_bf16_bits(self.seed, TID_Q, (self.B, self.Hq, self.q_len, self.d))

@@ -184,6 +184,25 @@ FA_API fa_status fa_flex_forward_mma(const void* q, const void* k, const void* v
                                      float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN,
                                      int32_t d, int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream);
 
+/* Gradients of fa_flex_forward's output ("5.1.2 FlexAttention ...", section 4.2: the backward reuses the
+ * BlockMask and its query-side transpose; FlashAttention self-test questions on the backward pass).
+ * With P recomputed from the forward's LSE and the score rule: D = rowsum(dout * out), dV = P^T dout,
+ * dS = P (dout V^T - D) times the soft-cap's chain factor, dQ = scale dS K, dK = scale dS^T Q; dK and dV
+ * summed over the query heads sharing a KV head (no atomics: one pass over the BlockMask rows for dQ, one
+ * over its columns for dK / dV).
+ *   q, k, v, block_mask, score_rule, scale, B .. d   as given to fa_flex_forward
+ *   out, out_dtype, lse   the forward's outputs (device; out bf16 or fp32 per out_dtype)
+ *   dout                  device bf16 [B,Hq,Q_LEN,d], the gradient of the loss with respect to out
+ *   dq, dk, dv            device fp32 [B,Hq,Q_LEN,d], [B,Hkv,KV_LEN,d], [B,Hkv,KV_LEN,d]; overwritten
+ *   delta                 device fp32 [B,Hq,Q_LEN] scratch (overwritten)
+ * Block sizes 64 or 128 (both dimensions), d in {64, 128}. Pointers 16-byte aligned. Errors as for
+ * fa_flex_forward; nothing is launched on an argument error. */
+FA_API fa_status fa_flex_backward(const void* q, const void* k, const void* v, const void* out, int32_t out_dtype,
+                                  const void* dout, const float* lse, const fa_block_mask* block_mask,
+                                  const fa_score_rule* score_rule, float scale, float* dq, float* dk, float* dv,
+                                  float* delta, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN,
+                                  int32_t d, int32_t* dev_status, fa_stream_t stream);
+
 /* Paged split-KV decode ("5.1.2 FlexAttention ...", sections 3.2 "split-KV exact merge" and 5.1-5.2;
  * "FlexAttention: compiler optimisation ...", section 6; the merge law of "5 Kernels ...", section 3).
  * One query token per request. Logical KV block c of request b lives in physical page
