@@ -37,6 +37,9 @@ def parse():
     p.add_argument("--decode-only", action="store_true",
                    help="time only the paged decode and print its object as the line (profiling aid)")
     p.add_argument("--decode-requests", type=int, default=64, help="requests in the decode batch")
+    p.add_argument("--no-backward", action="store_true")
+    p.add_argument("--backward-only", action="store_true",
+                   help="after the forward, time only the backward and print its object as the line (profiling aid)")
     return p.parse_args()
 
 
@@ -335,6 +338,15 @@ def ours(args, rank, world, local_rank):
         e2e = {"value": world * phys_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
 
+    # ---------------- backward over the same mask and forward outputs (secondary line item)
+    bwd_line = None
+    if not args.no_backward:
+        bwd_line = bench_backward(args, dev, pk, w, q, k, v, bm, sc, out, lse, phys_flops)
+        if args.backward_only:
+            if rank == 0:
+                print(json.dumps(bwd_line), flush=True)
+            return
+
     # ---------------- decode (secondary metric of the same hot path): paged split-KV, 64 requests
     dec_line = None
     if not args.no_decode:
@@ -375,10 +387,51 @@ def ours(args, rank, world, local_rank):
     }
     if dec_line:
         line["decode"] = dec_line
+    if bwd_line:
+        line["backward"] = bwd_line
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def bench_backward(args, dev, pk, w, q, k, v, bm, sc, out, lse, phys_flops):
+    """fa_flex_backward (delta, dQ and dK/dV kernels) on the forward's own mask, O and LSE. Algorithmic
+    FLOPs are 2.5x the forward's visited-block FLOPs (S recompute, dP, dV, dK, dQ: five d-deep products
+    per visited pair against the forward's two)."""
+    import torch
+
+    from block_sparse_masked_create_gb300 import fa, workloads
+    dout = workloads.bf16_torch(w.dout_bits(), dev)
+    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+    delta = torch.empty(lse.shape, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def bwd():
+        fa.flex_backward(q, k, v, out, lse, dout, bm, sc, w.scale, dq=dq, dk=dk, dv=dv, delta=delta, status=status)
+
+    for _ in range(3):
+        bwd()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    n = max(3, args.steps // 2)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        a.record(stream)
+        bwd()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    med = statistics.median(ms)
+    flop = 2.5 * phys_flops
+    tf = flop / (med * 1e-3) / 1e12
+    return {"workload": f"{w.name} backward: dout ~ N(0,1) bf16, dq/dk/dv fp32",
+            "kernels": "delta + dQ (row lists) + dK/dV (query-side transpose), mma.sync m16n8k16",
+            "ms_median": med, "algorithmic_tflop": flop / 1e12, "tflops": tf, "pct_bf16_peak": tf / pk["bf16"],
+            "peak_src": f"{pk['src']} bf16 burst", "launches_per_step": 3,
+            "status": fa.status_string(fa.check_status(status))}
 
 
 def bench_decode(args, dev, pk):
