@@ -150,6 +150,117 @@ __device__ __forceinline__ uint8_t classify_block(const DevRule& R, int64_t g0, 
   return R.n_terms > 1 ? kUnknown : FA_BLOCK_PARTIAL;
 }
 
+// Hull of a table row (or column): ascending, disjoint intervals of block indices that hold every block
+// with at least one allowed pair, so that blocks outside them are empty without being looked at (the
+// structured interval builder of "5.1.2 FlexAttention: from rules to fused kernels", section 2.2: for
+// interval rules the work is proportional to the visited blocks, not to nq x nk). Per OR-term the
+// allowed keys of a row range [g0, g1) (global positions) lie in one interval: "j < pre" bounds it
+// above, causal (j <= i) by g1, a window (i - j < W) below by g0 - W + 1, and document equality, where
+// the ids never decrease and the rows lie inside the id array with a non-negative first id, by the
+// runs of the first and last row. The same reasoning bounds the rows of a column range. Conservative
+// by construction: the blocks inside still go through the exact classification.
+struct Hull {
+  int n;
+  int lo[FA_MAX_RULE_TERMS], hi[FA_MAX_RULE_TERMS], pre[FA_MAX_RULE_TERMS + 1];
+};
+
+constexpr int64_t kHullWinMax = (int64_t)1 << 40;  // wider windows bound nothing at int32 lengths
+
+// add positions [lo, hi) (lo >= 0) as blocks of size bs, clipped to [0, nblk), keeping the list sorted
+__device__ void hull_add(Hull& h, int64_t lo, int64_t hi, int bs, int nblk) {
+  if (hi <= lo) return;
+  const int a = (int)(lo / bs);
+  const int b = (int)min((hi + bs - 1) / bs, (int64_t)nblk);
+  if (b <= a) return;
+  int k = h.n++;
+  while (k > 0 && h.lo[k - 1] > a) {
+    h.lo[k] = h.lo[k - 1];
+    h.hi[k] = h.hi[k - 1];
+    --k;
+  }
+  h.lo[k] = a;
+  h.hi[k] = b;
+}
+
+__device__ void hull_merge(Hull& h) {
+  int m = 0;
+  for (int k = 0; k < h.n; ++k) {
+    if (m > 0 && h.lo[k] <= h.hi[m - 1]) {
+      h.hi[m - 1] = max(h.hi[m - 1], h.hi[k]);
+    } else {
+      h.lo[m] = h.lo[k];
+      h.hi[m] = h.hi[k];
+      ++m;
+    }
+  }
+  h.n = m;
+  h.pre[0] = 0;
+  for (int k = 0; k < m; ++k) h.pre[k + 1] = h.pre[k] + h.hi[k] - h.lo[k];
+}
+
+// block index of the v-th block of the hull (v < pre[n])
+__device__ __forceinline__ int hull_at(const Hull& h, int v) {
+  int k = 0;
+  while (k + 1 < h.n && v >= h.pre[k + 1]) ++k;
+  return h.lo[k] + v - h.pre[k];
+}
+
+// KV blocks that rows [g0, g1) (global positions) can reach
+__device__ void row_hull(const DevRule& R, int bm, int64_t g0, int64_t g1, int64_t kv_len, int Bk, int nk,
+                         Hull& h) {
+  h.n = 0;
+  if (g1 > g0) {
+    bool refine = false;
+    int64_t rlo = 0, rhi = 0, unused = 0;
+    if (R.any_doc && doc_runs_usable(R, bm) && g0 >= 0 && g1 <= R.doc_len && doc_at(R, bm, g0) >= 0) {
+      doc_run_of(R, bm, g0, rlo, unused);
+      doc_run_of(R, bm, g1 - 1, unused, rhi);
+      refine = true;
+    }
+    for (int t = 0; t < R.n_terms; ++t) {
+      const DevTerm T = R.t[t];
+      int64_t lo = 0, hi = kv_len;
+      if (T.pre != INT64_MAX) hi = min(hi, T.pre);
+      if (T.causal) hi = min(hi, g1);
+      if (T.win != INT64_MAX && T.win < kHullWinMax) lo = max(lo, g0 - T.win + 1);
+      if (T.doc && refine) {
+        lo = max(lo, rlo);
+        hi = min(hi, rhi);
+      }
+      hull_add(h, lo, hi, Bk, nk);
+    }
+  }
+  hull_merge(h);
+}
+
+// query blocks (local rows, offset off to global) that can reach keys [j0, j1)
+__device__ void col_hull(const DevRule& R, int bm, int64_t off, int64_t j0, int64_t j1, int64_t q_len, int Bq,
+                         int nq, Hull& h) {
+  h.n = 0;
+  if (j1 > j0) {
+    bool refine = false;
+    int64_t clo = 0, chi = 0, unused = 0;
+    if (R.any_doc && doc_runs_usable(R, bm) && j1 <= R.doc_len && doc_at(R, bm, j0) >= 0) {
+      doc_run_of(R, bm, j0, clo, unused);
+      doc_run_of(R, bm, j1 - 1, unused, chi);
+      refine = true;
+    }
+    for (int t = 0; t < R.n_terms; ++t) {
+      const DevTerm T = R.t[t];
+      if (T.pre != INT64_MAX && j0 >= T.pre) continue;
+      int64_t lo = 0, hi = q_len;
+      if (T.causal) lo = max(lo, j0 - off);
+      if (T.win != INT64_MAX && T.win < kHullWinMax) hi = min(hi, j1 - 1 + T.win - off);
+      if (T.doc && refine) {
+        lo = max(lo, clo - off);
+        hi = min(hi, chi - off);
+      }
+      hull_add(h, max(lo, (int64_t)0), hi, Bq, nq);
+    }
+  }
+  hull_merge(h);
+}
+
 __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, MaskOut T) {
   const int r = blockIdx.x, hm = blockIdx.y, bm = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -163,6 +274,9 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
   __shared__ int s_b[kChunk];  // column-block document maximum, then "some pair not allowed"
   __shared__ int s_tmp[8];
   __shared__ int s_doc[kDocStage];  // column document ids of the blocks visited side by side
+  __shared__ Hull s_h;               // the KV blocks this query block can reach
+
+  if (tid == 0) row_hull(R, bm, i0 + off, i1 + off, T.kv_len, Bk, nk, s_h);
 
   // document range of the query block's valid rows (ids that never decrease: first and last row)
   int rdmin = INT_MAX, rdmax = INT_MIN;
@@ -210,14 +324,23 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
   int32_t* full_idx = T.full_kv_idx + row * nk;
   uint8_t* cls_row = T.block_class + row * nk;
 
+  __syncthreads();
+  const int nh = s_h.pre[s_h.n];  // blocks in the hull; the rest are empty
+  for (int x = tid; x < nk; x += kThreads) {
+    bool in = false;
+    for (int k = 0; k < s_h.n; ++k) in = in || (x >= s_h.lo[k] && x < s_h.hi[k]);
+    if (!in) cls_row[x] = FA_BLOCK_EMPTY;
+  }
+  auto col = [&](int v) { return hull_at(s_h, v); };
+
   int run_p = 0, run_f = 0;
-  for (int c0 = 0; c0 < nk; c0 += kChunk) {
-    const int cn = min(kChunk, nk - c0);
+  for (int c0 = 0; c0 < nh; c0 += kChunk) {
+    const int cn = min(kChunk, nh - c0);
     // 1. document range of every column block of the chunk: first and last id when the ids never
     // decrease, else a warp per block (coalesced)
     if (sorted_ids) {
       for (int x = tid; x < cn; x += kThreads) {
-        const int64_t j0 = (int64_t)(c0 + x) * Bk;
+        const int64_t j0 = (int64_t)col(c0 + x) * Bk;
         const int64_t j1 = min(j0 + Bk, (int64_t)T.kv_len);
         s_a[x] = doc_at(R, bm, j0);
         s_b[x] = doc_at(R, bm, j1 - 1);
@@ -225,7 +348,7 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
       __syncthreads();
     } else if (R.any_doc) {
       for (int x = warp; x < cn; x += kThreads / 32) {
-        const int64_t j0 = (int64_t)(c0 + x) * Bk;
+        const int64_t j0 = (int64_t)col(c0 + x) * Bk;
         const int w = (int)min((int64_t)Bk, (int64_t)T.kv_len - j0);
         int mn = INT_MAX, mx = INT_MIN;
         for (int cc = lane; cc < w; cc += 32) {
@@ -248,7 +371,7 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
     // 2. block-level classification
     bool has_unknown = false;
     for (int x = tid; x < cn; x += kThreads) {
-      const int64_t j0 = (int64_t)(c0 + x) * Bk, j1 = min(j0 + Bk, (int64_t)T.kv_len);
+      const int64_t j0 = (int64_t)col(c0 + x) * Bk, j1 = min(j0 + Bk, (int64_t)T.kv_len);
       const uint8_t cl = classify_block(R, i0 + off, i1 + off, j0, j1, rows_full && j1 - j0 == Bk, rdmin, rdmax,
                                         R.any_doc ? s_a[x] : 0, R.any_doc ? s_b[x] : 0);
       s_cls[x] = cl;
@@ -271,14 +394,14 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
         if (stage) {
           for (int x = tid; x < lanes * Bk; x += kThreads) {
             const int cc = base + x / Bk;
-            const int64_t j = (int64_t)(c0 + cc) * Bk + x % Bk;
+            const int64_t j = (int64_t)col(c0 + cc) * Bk + x % Bk;
             s_doc[x] = (cc < cn && s_cls[cc] == kUnknown && j < T.kv_len) ? doc_at(R, bm, j) : 0;
           }
           __syncthreads();
         }
         const int cc = base + lam;
         if (active && cc < cn && s_cls[cc] == kUnknown) {
-          const int64_t j0 = (int64_t)(c0 + cc) * Bk;
+          const int64_t j0 = (int64_t)col(c0 + cc) * Bk;
           const int w = (int)min((int64_t)Bk, (int64_t)T.kv_len - j0);
           bool any = false, all = false;
           if (row_in) {
@@ -308,7 +431,7 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
     int np = 0, nf = 0;
     for (int x = s0; x < s1; ++x) {
       const uint8_t cl = s_cls[x];
-      cls_row[c0 + x] = cl;
+      cls_row[col(c0 + x)] = cl;
       np += cl == FA_BLOCK_PARTIAL;
       nf += cl == FA_BLOCK_FULL;
     }
@@ -316,8 +439,8 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
     int p = run_p + so.excl_a, f = run_f + so.excl_b;
     for (int x = s0; x < s1; ++x) {
       const uint8_t cl = s_cls[x];
-      if (cl == FA_BLOCK_PARTIAL) kv_idx[p++] = c0 + x;
-      if (cl == FA_BLOCK_FULL) full_idx[f++] = c0 + x;
+      if (cl == FA_BLOCK_PARTIAL) kv_idx[p++] = col(c0 + x);
+      if (cl == FA_BLOCK_FULL) full_idx[f++] = col(c0 + x);
     }
     run_p += so.tot_a;
     run_f += so.tot_b;
@@ -331,33 +454,42 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
   }
 }
 
-__global__ void __launch_bounds__(kThreads) mask_transpose_kernel(MaskOut T) {
+__global__ void __launch_bounds__(kThreads) mask_transpose_kernel(DevRule R, MaskOut T) {
   const int c = blockIdx.x, hm = blockIdx.y, bm = blockIdx.z;
   const int tid = threadIdx.x;
   const int nq = T.nq, nk = T.nk;
   __shared__ int s_tmp[8];
+  __shared__ Hull s_h;  // the query blocks that can reach this KV block; the class matrix is empty elsewhere
+  if (tid == 0) {
+    const int64_t off = R.q_offset ? (int64_t)__ldg(R.q_offset + bm) : 0;
+    const int64_t j0 = (int64_t)c * T.bk, j1 = min(j0 + T.bk, (int64_t)T.kv_len);
+    col_hull(R, bm, off, j0, j1, T.q_len, T.bq, nq, s_h);
+  }
+  __syncthreads();
+  const int nh = s_h.pre[s_h.n];
   const size_t head = (size_t)bm * T.Hm + hm;
   const uint8_t* cls = T.block_class + head * nq * nk + c;  // column c, stride nk
   const size_t col = head * nk + c;
   int32_t* q_idx = T.q_idx + col * nq;
   int32_t* fq_idx = T.full_q_idx + col * nq;
   int run_p = 0, run_f = 0;
-  for (int r0 = 0; r0 < nq; r0 += kChunk) {
-    const int rn = min(kChunk, nq - r0);
+  for (int r0 = 0; r0 < nh; r0 += kChunk) {
+    const int rn = min(kChunk, nh - r0);
     const int seg = (rn + kThreads - 1) / kThreads;
     const int s0 = min(tid * seg, rn), s1 = min(s0 + seg, rn);
     int np = 0, nf = 0;
     for (int x = s0; x < s1; ++x) {
-      const uint8_t cl = cls[(size_t)(r0 + x) * nk];
+      const uint8_t cl = cls[(size_t)hull_at(s_h, r0 + x) * nk];
       np += cl == FA_BLOCK_PARTIAL;
       nf += cl == FA_BLOCK_FULL;
     }
     ScanOut so = block_scan2(np, nf, s_tmp);
     int p = run_p + so.excl_a, f = run_f + so.excl_b;
     for (int x = s0; x < s1; ++x) {
-      const uint8_t cl = cls[(size_t)(r0 + x) * nk];
-      if (cl == FA_BLOCK_PARTIAL) q_idx[p++] = r0 + x;
-      if (cl == FA_BLOCK_FULL) fq_idx[f++] = r0 + x;
+      const int r = hull_at(s_h, r0 + x);
+      const uint8_t cl = cls[(size_t)r * nk];
+      if (cl == FA_BLOCK_PARTIAL) q_idx[p++] = r;
+      if (cl == FA_BLOCK_FULL) fq_idx[f++] = r;
     }
     run_p += so.tot_a;
     run_f += so.tot_b;
@@ -370,7 +502,6 @@ __global__ void __launch_bounds__(kThreads) mask_transpose_kernel(MaskOut T) {
   }
 }
 
-// dev_out = {full, partial, empty, max row length, sum of row lengths, rows} (zeroed by the launcher)
 __global__ void __launch_bounds__(256) mask_stats_kernel(MaskOut T, unsigned long long* out) {
   const long long rows = (long long)T.Bm * T.Hm * T.nq;
   long long f = 0, p = 0, mx = 0;
@@ -420,7 +551,7 @@ cudaError_t launch_mask_build(const DevRule& R0, const MaskOut& T, cudaStream_t 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 g2(T.nk, T.Hm, T.Bm);
-  mask_transpose_kernel<<<g2, kThreads, 0, st>>>(T);
+  mask_transpose_kernel<<<g2, kThreads, 0, st>>>(R, T);
   return cudaGetLastError();
 }
 

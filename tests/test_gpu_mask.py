@@ -159,3 +159,73 @@ def test_cfg5_decode_table():
     dp = workloads.cfg5(prefix=512)
     _, tp = gpu_tables(dp.rule, dp.Bz, dp.Hq, 1, dp.kv_len, 1, dp.page, q_off=off, bdep=True)
     assert_tables_equal(tp, t)      # the prefix region is already visible at every cur_pos >= 1023
+
+
+def _random_rule(rng):
+    """An OR of one to three AND-terms over causal / window / prefix / document atoms."""
+    def atom():
+        k = rng.integers(0, 4)
+        if k == 0:
+            return [("causal",)]
+        if k == 1:
+            return [("window", int(rng.integers(1, 90)))]
+        if k == 2:
+            return [("prefix", int(rng.integers(0, 120)))]
+        return [("doc",)]
+
+    def term():  # at most 3 ops, so a rule stays within 16 ops and 8 OR-terms
+        ops = atom()
+        for _ in range(int(rng.integers(0, 2))):
+            ops += atom() + [("and",)]
+        return ops
+
+    spec = term()
+    for _ in range(int(rng.integers(0, 3))):
+        spec += term() + [("or",)]
+    return spec
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_hull_random_rules(seed):
+    # the builder skips blocks outside each row's (column's) interval hull: random OR / AND rules over
+    # many blocks, per-request query offsets (which push rows past the end of the id array), sorted ids
+    # with a leading -1 run, and unsorted ids on some seeds
+    rng = np.random.default_rng(7000 + seed)
+    spec = _random_rule(rng)
+    B = 2
+    q_len, kv_len = int(rng.integers(1, 500)), int(rng.integers(1, 700))
+    bq, bk = int(rng.choice([1, 8, 16, 64, 128])), int(rng.choice([4, 16, 32, 128]))
+    off = rng.integers(0, 300, size=B).astype(np.int32)
+    n_doc = kv_len + int(rng.integers(0, 400))  # ids cover the keys; offset rows may pass the end
+    doc = np.sort(rng.integers(-1, 12, size=(B, n_doc)), axis=1).astype(np.int32)
+    if seed % 5 == 4:
+        rng.shuffle(doc, axis=1)
+    uses_doc = any(op[0] == "doc" for op in spec)
+    _, t = gpu_tables(spec, B, 1, q_len, kv_len, bq, bk, doc=doc if uses_doc else None, q_off=off, bdep=True)
+    want = orc.block_mask(spec, B, 1, q_len, kv_len, bq, bk, batch_dependent=True, q_offset=off,
+                          doc_ids=doc if uses_doc else None)
+    assert_tables_equal(t, want)
+
+
+def test_long_window_table_o_visited():
+    # N = 262144, causal window 1024, 128x128 blocks: 2048 x 2048 blocks of which ~9 per row are
+    # visited. Counts by closed form, sampled rows and columns against the oracle.
+    N, W, bs = 262144, 1024, 128
+    spec = CW(W)
+    bm, t = gpu_tables(spec, 1, 1, N, N, bs, bs)
+    nb = N // bs
+    st = fa.block_mask_stats(bm).cpu().tolist()
+    # row r >= 8: blocks r-8 (partial), r-7 .. r-1 (full), r (partial); rows 0..7 fewer
+    full = sum(max(0, min(r, 7)) for r in range(nb))
+    partial = sum(1 + (r >= 8) for r in range(nb))
+    assert (st[0], st[1], st[3]) == (full, partial, 9)
+    rows = [0, 1, 7, 8, 9, 1000, 2046, 2047]
+    want = orc.block_mask(spec, 1, 1, N, N, bs, bs, rows=rows)
+    assert_tables_equal(t, want, rows=rows)
+    for c in (0, 5, 1000, 2040, 2047):
+        # the query-side transpose of column c: rows c and c+8 partial, c+1 .. c+7 full (clipped)
+        want_p = [r for r in (c, c + 8) if r < nb]
+        want_f = list(range(c + 1, min(c + 8, nb)))
+        assert t["q_idx"][0, 0, c, :t["q_num"][0, 0, c]].tolist() == want_p
+        assert t["full_q_idx"][0, 0, c, :t["full_q_num"][0, 0, c]].tolist() == want_f
+        assert not t["q_idx"][0, 0, c, len(want_p):].any() and not t["full_q_idx"][0, 0, c, len(want_f):].any()
