@@ -239,14 +239,23 @@ static int check_forward(const void* q, const void* k, const void* v, const fa_b
   return FA_OK;
 }
 
+struct PagedKV {  // all zero: contiguous K / V
+  const int32_t* page_table;
+  int32_t n_pages_total, page, max_pages;
+};
+
 static int forward_impl(bool force_mma, const void* q, const void* k, const void* v, const fa_block_mask* bm,
                         const fa_score_rule* score, float scale, void* out, int32_t out_dtype, float* lse,
                         int32_t B, int32_t Hq,
                         int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d, int32_t* dev_status,
-                        int64_t* dev_counters, fa_stream_t stream) {
+                        int64_t* dev_counters, fa_stream_t stream, const PagedKV& pg = PagedKV{}) {
   int s = check_forward(q, k, v, bm, out, lse, B, Hq, Hkv, Q_LEN, KV_LEN, d);
   if (s != FA_OK) return s;
   if (out_dtype != FA_OUT_BF16 && out_dtype != FA_OUT_F32) return FA_ERR_INVALID_ARG;
+  if (pg.page_table) {  // one page per key block; the table covers every key block
+    if (pg.page != bm->bk || pg.n_pages_total < 1 || pg.max_pages < bm->nk) return FA_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(pg.page_table) & 3u) return FA_ERR_INVALID_ARG;
+  }
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
   s = compile_rule(&bm->rule, &a.rule);
@@ -271,6 +280,9 @@ static int forward_impl(bool force_mma, const void* q, const void* k, const void
   a.status = dev_status;
   a.counters = dev_counters;
   a.timeout_ns = g_timeout_ns.load();
+  a.page_table = pg.page_table;
+  a.max_pages = pg.max_pages;
+  a.n_pages_total = pg.n_pages_total;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (!force_mma && bm->bq == 128 && bm->bk == 128) {
     int r = launch_fwd_tc5(a, st);
@@ -417,12 +429,123 @@ fa_status fa_create_block_mask(const fa_mask_rule* rule, int32_t B, int32_t H, i
   return FA_OK;
 }
 
+// Layout of the one-row-per-request mask fa_block_mask_select_rows writes: Bm = Bz, Hm = src->Hm, nq = 1.
+static int select_layout(const fa_block_mask* src, int32_t Bz, MaskLayout* L) {
+  if (!src || Bz < 1) return FA_ERR_INVALID_ARG;
+  if (src->nq < 1 || src->nk < 1 || src->Hm < 1 || src->bk < 1) return FA_ERR_SHAPE;
+  if (src->Bm != 1 && src->Bm != Bz) return FA_ERR_SHAPE;
+  fa_mask_rule r;
+  std::memset(&r, 0, sizeof(r));
+  r.n_ops = 1;
+  r.op[0] = FA_M_TRUE;
+  r.batch_dependent = 1;
+  r.head_dependent = src->Hm > 1;
+  return mask_layout(&r, Bz, src->Hm, 1, src->kv_len, 1, src->bk, L);
+}
+
+size_t fa_block_mask_select_bytes(const fa_block_mask* src, int32_t Bz) {
+  MaskLayout L;
+  return select_layout(src, Bz, &L) == FA_OK ? L.total : 0;
+}
+
+fa_status fa_block_mask_select_rows(const fa_block_mask* src, const int32_t* dev_q_pos, int32_t Bz, void* dev_buf,
+                                    size_t buf_bytes, fa_block_mask* out, int32_t* dev_status, fa_stream_t stream) {
+  if (!src || !dev_q_pos || !dev_buf || !out) return FA_ERR_INVALID_ARG;
+  if (src->rule.q_offset) return FA_ERR_INVALID_ARG;  // the prebuilt table must be in global positions
+  if (!src->kv_num || !src->kv_idx || !src->full_kv_num || !src->full_kv_idx || !src->block_class)
+    return FA_ERR_INVALID_ARG;
+  MaskLayout L;
+  int s = select_layout(src, Bz, &L);
+  if (s != FA_OK) return (fa_status)s;
+  if (buf_bytes < L.total) return FA_ERR_BUFFER_TOO_SMALL;
+  if (reinterpret_cast<uintptr_t>(dev_buf) & 255u) return FA_ERR_INVALID_ARG;
+  if (Bz > 65535 || src->Hm > 65535) return FA_ERR_UNSUPPORTED;
+  MaskOut S;
+  std::memset(&S, 0, sizeof(S));
+  S.Bm = src->Bm;
+  S.Hm = src->Hm;
+  S.q_len = src->q_len;
+  S.kv_len = src->kv_len;
+  S.bq = src->bq;
+  S.bk = src->bk;
+  S.nq = src->nq;
+  S.nk = src->nk;
+  S.kv_num = src->kv_num;
+  S.kv_idx = src->kv_idx;
+  S.full_kv_num = src->full_kv_num;
+  S.full_kv_idx = src->full_kv_idx;
+  S.block_class = src->block_class;
+  uint8_t* base = static_cast<uint8_t*>(dev_buf);
+  MaskOut D;
+  std::memset(&D, 0, sizeof(D));
+  D.Bm = Bz;
+  D.Hm = src->Hm;
+  D.q_len = 1;
+  D.kv_len = src->kv_len;
+  D.bq = 1;
+  D.bk = src->bk;
+  D.nq = 1;
+  D.nk = src->nk;
+  D.kv_num = reinterpret_cast<int32_t*>(base + L.off[0]);
+  D.full_kv_num = reinterpret_cast<int32_t*>(base + L.off[1]);
+  D.q_num = reinterpret_cast<int32_t*>(base + L.off[2]);
+  D.full_q_num = reinterpret_cast<int32_t*>(base + L.off[3]);
+  D.kv_idx = reinterpret_cast<int32_t*>(base + L.off[4]);
+  D.full_kv_idx = reinterpret_cast<int32_t*>(base + L.off[5]);
+  D.q_idx = reinterpret_cast<int32_t*>(base + L.off[6]);
+  D.full_q_idx = reinterpret_cast<int32_t*>(base + L.off[7]);
+  D.block_class = base + L.off[8];
+  DevRule R;
+  s = compile_rule(&src->rule, &R);
+  if (s != FA_OK) return (fa_status)s;
+  R.q_offset = dev_q_pos;
+  R.doc_run = src->doc_run;
+  R.doc_sorted = src->doc_sorted;
+  if (R.any_doc && src->rule.doc_batch != 1 && src->rule.doc_batch != Bz) return FA_ERR_SHAPE;
+  if (launch_mask_select(R, S, Bz, D, dev_status, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  out->Bm = D.Bm;
+  out->Hm = D.Hm;
+  out->q_len = 1;
+  out->kv_len = D.kv_len;
+  out->bq = 1;
+  out->bk = D.bk;
+  out->nq = 1;
+  out->nk = D.nk;
+  out->kv_num = D.kv_num;
+  out->kv_idx = D.kv_idx;
+  out->full_kv_num = D.full_kv_num;
+  out->full_kv_idx = D.full_kv_idx;
+  out->q_num = D.q_num;
+  out->q_idx = D.q_idx;
+  out->full_q_num = D.full_q_num;
+  out->full_q_idx = D.full_q_idx;
+  out->block_class = D.block_class;
+  out->doc_run = src->doc_run;  // same document ids, same runs
+  out->doc_sorted = src->doc_sorted;
+  out->rule = src->rule;
+  out->rule.q_offset = dev_q_pos;  // the one query row of request b sits at global position q_pos[b]
+  out->rule.batch_dependent = 1;
+  return FA_OK;
+}
+
 fa_status fa_flex_forward(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
                           const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype, float* lse,
                           int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d,
                           int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream) {
   return (fa_status)forward_impl(false, q, k, v, block_mask, score_rule, scale, out, out_dtype, lse, B, Hq, Hkv, Q_LEN,
                                  KV_LEN, d, dev_status, dev_counters, stream);
+}
+
+fa_status fa_flex_forward_paged(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                                int32_t n_pages_total, int32_t page, int32_t max_pages,
+                                const fa_block_mask* block_mask, const fa_score_rule* score_rule, float scale,
+                                void* out, int32_t out_dtype, float* lse, int32_t B, int32_t Hq, int32_t Hkv,
+                                int32_t Q_LEN, int32_t KV_LEN, int32_t d, int32_t* dev_status, fa_stream_t stream) {
+  if (!page_table) return FA_ERR_INVALID_ARG;
+  return (fa_status)forward_impl(false, q, k_pages, v_pages, block_mask, score_rule, scale, out, out_dtype, lse, B,
+                                 Hq, Hkv, Q_LEN, KV_LEN, d, dev_status, nullptr, stream,
+                                 PagedKV{page_table, n_pages_total, page, max_pages});
 }
 
 fa_status fa_flex_forward_mma(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,

@@ -39,6 +39,10 @@ struct MaskOut {
 
 cudaError_t launch_mask_build(const DevRule& R, const MaskOut& T, cudaStream_t st);
 cudaError_t launch_mask_stats(const MaskOut& T, int64_t* dev_out, cudaStream_t st);
+// row block q_pos[b] / S.bq of S per request b, re-classified at position q_pos[b] = R.q_offset[b] -> D with
+// Bm = Bz, nq = 1 (D's buffers laid out by the caller)
+cudaError_t launch_mask_select(const DevRule& R, const MaskOut& S, int Bz, const MaskOut& D, int32_t* status,
+                               cudaStream_t st);
 
 struct FwdArgs {
   const void* q;
@@ -55,6 +59,10 @@ struct FwdArgs {
   int32_t* status;
   int64_t* counters;
   uint64_t timeout_ns;
+  // paged K/V (NULL: contiguous [B, Hkv, kv_len, d]): k and v point at pages [n_pages_total, Hkv, Bk, d]
+  // and key block c of batch row b lives in page page_table[b * max_pages + c] (one page per key block)
+  const int32_t* page_table;
+  int32_t max_pages, n_pages_total;
 };
 
 cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t st);

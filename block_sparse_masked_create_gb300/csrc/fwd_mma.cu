@@ -96,12 +96,26 @@ __global__ void __launch_bounds__(MmaCfg<D, BQ, BK>::kThreads)
     const int c = n < n_full ? __ldg(full_idx + n) : __ldg(part_idx + n - n_full);
     const int j0 = c * BK;
     uint32_t kb = smem_u32(sK + stage * C::kKVBytes), vb = smem_u32(sV + stage * C::kKVBytes);
+    const __nv_bfloat16* Kb = Kg;  // rows of the block start at Kb + row * D
+    const __nv_bfloat16* Vb = Vg;
+    int rbase = j0;
+    if (a.page_table) {  // key block c is one whole page of BK rows; a bad id is reported and page 0 read
+      int pg = __ldg(a.page_table + (size_t)b * a.max_pages + c);
+      if (pg < 0 || pg >= a.n_pages_total) {
+        if (tid == 0) report(a.status, FA_ERR_DEVICE_CHECK);
+        pg = 0;
+      }
+      const size_t page_off = ((size_t)pg * a.Hkv + hk) * BK * D;
+      Kb = reinterpret_cast<const __nv_bfloat16*>(a.k) + page_off;
+      Vb = reinterpret_cast<const __nv_bfloat16*>(a.v) + page_off;
+      rbase = 0;
+    }
     for (int x = tid; x < BK * kChunks; x += C::kThreads) {
       int rr = x / kChunks, ch = x % kChunks;
       bool ok = j0 + rr < a.kv_len;
-      size_t off = (size_t)(ok ? j0 + rr : 0) * D + ch * 8;
-      cp_async_16(kb + swz<D>(rr, ch), Kg + off, ok);
-      cp_async_16(vb + swz<D>(rr, ch), Vg + off, ok);
+      size_t off = (size_t)(ok ? rbase + rr : 0) * D + ch * 8;
+      cp_async_16(kb + swz<D>(rr, ch), Kb + off, ok);
+      cp_async_16(vb + swz<D>(rr, ch), Vb + off, ok);
     }
   };
 

@@ -176,11 +176,21 @@ __global__ void __launch_bounds__(Roles<NT>::kThreads, Roles<NT>::kCtasPerSm)
   auto load_slot = [&](const Tile& T, bool is_v, int j) {  // into the next slot, which must be free
     const int s = issued % NST;
     const int c = T.col(j);
+    int yk = c * 128, zk = b * a.Hkv + T.hk;
+    if (a.page_table) {  // key block c is one whole page; a bad page id is reported and page 0 read instead
+      int pg = __ldg(a.page_table + (size_t)b * a.max_pages + c);
+      if (pg < 0 || pg >= a.n_pages_total) {
+        if (lane == 0) report(a.status, FA_ERR_DEVICE_CHECK);
+        pg = 0;
+      }
+      yk = 0;
+      zk = pg * a.Hkv + T.hk;
+    }
     uint8_t* dst = sRing + s * C::kSlotBytes;
     mbar_arrive_expect_tx_elect(&bar_full[s], C::kSlotBytes);
 #pragma unroll
     for (int x = 0; x < D / 64; ++x)
-      tma_load_3d_elect(dst + x * 16384, is_v ? &tmV : &tmK, x * 64, c * 128, b * a.Hkv + T.hk, &bar_full[s]);
+      tma_load_3d_elect(dst + x * 16384, is_v ? &tmV : &tmK, x * 64, yk, zk, &bar_full[s]);
     ++issued;
   };
   if (warp == kLoadWarp) {
@@ -709,9 +719,12 @@ int launch_k(const FwdArgs& a, cudaStream_t st) {
   using C = Tc5Cfg<D, NT>;
   CUtensorMap tq, tk, tv, to;
   const uint64_t dq[3] = {(uint64_t)D, (uint64_t)a.q_len, (uint64_t)a.B * a.Hq};
-  const uint64_t dk[3] = {(uint64_t)D, (uint64_t)a.kv_len, (uint64_t)a.B * a.Hkv};
+  // K / V: [B * Hkv, kv_len, D], or pages [n_pages_total * Hkv, 128, D] read one whole page per block
+  const bool paged = a.page_table != nullptr;
+  const uint64_t dk[3] = {(uint64_t)D, paged ? 128u : (uint64_t)a.kv_len,
+                          paged ? (uint64_t)a.n_pages_total * a.Hkv : (uint64_t)a.B * a.Hkv};
   const uint64_t sq[2] = {(uint64_t)D * 2, (uint64_t)a.q_len * D * 2};
-  const uint64_t sk[2] = {(uint64_t)D * 2, (uint64_t)a.kv_len * D * 2};
+  const uint64_t sk[2] = {(uint64_t)D * 2, (paged ? 128u : (uint64_t)a.kv_len) * D * 2};
   const uint32_t box[3] = {64, 128, 1};
   if (encode_tmap_bf16(&tq, a.q, 3, dq, sq, box) || encode_tmap_bf16(&tk, a.k, 3, dk, sk, box) ||
       encode_tmap_bf16(&tv, a.v, 3, dk, sk, box))

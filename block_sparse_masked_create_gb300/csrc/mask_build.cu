@@ -533,6 +533,80 @@ __global__ void mask_stats_finish(MaskOut T, unsigned long long* out) {
   out[2] = total - out[0] - out[1];
 }
 
+// One row of a prebuilt table per request ("5.1.2 FlexAttention ...", section 5.2: build the table once
+// for the longest context, then at each decode step take the query block that holds each request's
+// position and keep the exact rule for its partial blocks). One CTA per (request, h_m). The block row's
+// full and empty blocks are full / empty for each of its valid rows, so only its partial blocks are
+// looked at again, for the one query row at the request's position: they become empty, full or stay
+// partial. The result is the table a one-row build at that position gives, without the classification
+// of the row's other blocks (for a paged cache this also drops blocks past the request's own length,
+// whose pages may not exist). A position outside [0, src q_len) reports a device-check error and yields
+// an empty row.
+__global__ void __launch_bounds__(kThreads) mask_select_kernel(DevRule R, MaskOut S, MaskOut D, int32_t* status) {
+  const int bz = blockIdx.x, hm = blockIdx.y, tid = threadIdx.x;
+  const int nk = S.nk, Bk = S.bk;
+  __shared__ uint8_t s_cls[kChunk];
+  __shared__ int s_tmp[8];
+  const int64_t pos = __ldg(R.q_offset + bz);
+  const bool ok = pos >= 0 && pos < S.q_len;
+  if (!ok && tid == 0) report(status, FA_ERR_DEVICE_CHECK);
+  const int sb = S.Bm > 1 ? bz : 0;
+  const size_t srow = ((size_t)sb * S.Hm + hm) * S.nq + (ok ? pos / S.bq : 0);
+  const size_t drow = (size_t)bz * D.Hm + hm;  // nq = 1
+  const int doc_i = (R.any_doc && ok) ? doc_at(R, bz, pos) : -1;
+  const Bits128 full_bk = range_bits(0, Bk);
+  int run_p = 0, run_f = 0;
+  for (int c0 = 0; c0 < nk; c0 += kChunk) {
+    const int cn = min(kChunk, nk - c0);
+    for (int x = tid; x < cn; x += kThreads) {
+      uint8_t cl = ok ? S.block_class[srow * nk + c0 + x] : (uint8_t)FA_BLOCK_EMPTY;
+      if (cl == FA_BLOCK_PARTIAL) {
+        const int64_t j0 = (int64_t)(c0 + x) * Bk;
+        const int w = (int)min((int64_t)Bk, (int64_t)S.kv_len - j0);
+        const Bits128 bits = rule_row_bits(R, pos, j0, w, doc_i, [&](int d) {
+          return doc_bits<4>(w, d, [&](int c) { return doc_at(R, bz, j0 + c); });
+        });
+        const bool any = (bits.w[0] | bits.w[1] | bits.w[2] | bits.w[3]) != 0u;
+        const bool all = w == Bk && bits.w[0] == full_bk.w[0] && bits.w[1] == full_bk.w[1] &&
+                         bits.w[2] == full_bk.w[2] && bits.w[3] == full_bk.w[3];
+        cl = any ? (all ? FA_BLOCK_FULL : FA_BLOCK_PARTIAL) : FA_BLOCK_EMPTY;
+      }
+      s_cls[x] = cl;
+    }
+    __syncthreads();
+    const int seg = (cn + kThreads - 1) / kThreads;
+    const int s0 = min(tid * seg, cn), s1 = min(s0 + seg, cn);
+    int np = 0, nf = 0;
+    for (int x = s0; x < s1; ++x) {
+      const uint8_t cl = s_cls[x];
+      const size_t e = drow * nk + c0 + x;
+      D.block_class[e] = cl;
+      D.q_num[e] = cl == FA_BLOCK_PARTIAL;  // the transpose of a one-row table
+      D.full_q_num[e] = cl == FA_BLOCK_FULL;
+      D.q_idx[e] = 0;
+      D.full_q_idx[e] = 0;
+      np += cl == FA_BLOCK_PARTIAL;
+      nf += cl == FA_BLOCK_FULL;
+    }
+    ScanOut so = block_scan2(np, nf, s_tmp);
+    int p = run_p + so.excl_a, f = run_f + so.excl_b;
+    for (int x = s0; x < s1; ++x) {
+      const uint8_t cl = s_cls[x];
+      if (cl == FA_BLOCK_PARTIAL) D.kv_idx[drow * nk + p++] = c0 + x;
+      if (cl == FA_BLOCK_FULL) D.full_kv_idx[drow * nk + f++] = c0 + x;
+    }
+    run_p += so.tot_a;
+    run_f += so.tot_b;
+    __syncthreads();
+  }
+  for (int x = run_p + tid; x < nk; x += kThreads) D.kv_idx[drow * nk + x] = 0;
+  for (int x = run_f + tid; x < nk; x += kThreads) D.full_kv_idx[drow * nk + x] = 0;
+  if (tid == 0) {
+    D.kv_num[drow] = run_p;
+    D.full_kv_num[drow] = run_f;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_mask_build(const DevRule& R0, const MaskOut& T, cudaStream_t st) {
@@ -552,6 +626,12 @@ cudaError_t launch_mask_build(const DevRule& R0, const MaskOut& T, cudaStream_t 
   if (e != cudaSuccess) return e;
   dim3 g2(T.nk, T.Hm, T.Bm);
   mask_transpose_kernel<<<g2, kThreads, 0, st>>>(R, T);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mask_select(const DevRule& R, const MaskOut& S, int Bz, const MaskOut& D, int32_t* status,
+                               cudaStream_t st) {
+  mask_select_kernel<<<dim3(Bz, D.Hm), kThreads, 0, st>>>(R, S, D, status);
   return cudaGetLastError();
 }
 

@@ -82,6 +82,13 @@ def load() -> ctypes.CDLL:
     lib.fa_flex_forward.argtypes = fwd_args
     lib.fa_flex_forward_mma.restype = ctypes.c_int
     lib.fa_flex_forward_mma.argtypes = fwd_args
+    lib.fa_block_mask_select_bytes.restype = sz
+    lib.fa_block_mask_select_bytes.argtypes = [P(BlockMaskC), i32]
+    lib.fa_block_mask_select_rows.restype = ctypes.c_int
+    lib.fa_block_mask_select_rows.argtypes = [P(BlockMaskC), vp, i32, vp, sz, P(BlockMaskC), vp, vp]
+    lib.fa_flex_forward_paged.restype = ctypes.c_int
+    lib.fa_flex_forward_paged.argtypes = [vp, vp, vp, vp, i32, i32, i32, P(BlockMaskC), P(ScoreRule), f32, vp, i32, vp,
+                                          i32, i32, i32, i32, i32, i32, vp, vp]
     lib.fa_flex_backward.restype = ctypes.c_int
     lib.fa_flex_backward.argtypes = [vp, vp, vp, vp, i32, vp, vp, P(BlockMaskC), P(ScoreRule), f32, vp, vp, vp, vp,
                                      i32, i32, i32, i32, i32, i32, vp, vp]
@@ -240,6 +247,27 @@ def recreate_block_mask(bm: BlockMask, rule: MaskRule, B: int, H: int, Q_LEN: in
                                        ctypes.byref(bm.c), _stream(bm.buf.device)), "fa_create_block_mask")
 
 
+def select_rows(src: BlockMask, q_pos: torch.Tensor, out: Optional[BlockMask] = None,
+                status: Optional[torch.Tensor] = None) -> BlockMask:
+    """fa_block_mask_select_rows: from a table prebuilt for the longest context (global positions), the row
+    block holding each request's query position q_pos[b] (device int32 [Bz]), as a one-row-per-request
+    mask (Bm = Bz, q_len = 1, Bq = 1) whose rule sees q_pos as the query offset. Reuses `out`'s buffer."""
+    if q_pos.dtype != torch.int32 or not q_pos.is_contiguous() or q_pos.dim() != 1:
+        raise ValueError("q_pos must be contiguous int32 [Bz]")
+    lib = load()
+    Bz = q_pos.shape[0]
+    n = int(lib.fa_block_mask_select_bytes(ctypes.byref(src.c), Bz))
+    if n == 0:
+        raise FaError(ERR_SHAPE, "fa_block_mask_select_bytes")
+    if out is None or out.buf.numel() < n:
+        out = BlockMask(BlockMaskC(), torch.empty(n, dtype=torch.uint8, device=src.buf.device), [])
+    out.keep = list(src.keep) + [src, q_pos]
+    _check(lib.fa_block_mask_select_rows(ctypes.byref(src.c), _ptr(q_pos), Bz, _ptr(out.buf), out.buf.numel(),
+                                         ctypes.byref(out.c), _ptr(status), _stream(out.buf.device)),
+           "fa_block_mask_select_rows")
+    return out
+
+
 def block_mask_stats(bm: BlockMask, out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """int64[6] on the device: full, partial, empty, max row length, sum of row lengths, rows."""
     if out is None:
@@ -279,6 +307,32 @@ def flex_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: 
     _check(fn(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(block_mask.c), ctypes.byref(score) if score else None,
               float(scale) if scale else 0.0, _ptr(out), _out_code(out), _ptr(lse), B, Hq, Hkv, Q_LEN, KV_LEN, d,
               _ptr(status), _ptr(counters), _stream(q.device)), "fa_flex_forward")
+    return out, lse
+
+
+def flex_forward_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, page_table: torch.Tensor,
+                       block_mask: BlockMask, KV_LEN: int, score: Optional[ScoreRule] = None,
+                       scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                       lse: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                       out_dtype=torch.bfloat16):
+    """fa_flex_forward_paged: q [B,Hq,Q_LEN,d]; k/v pages [P,Hkv,page,d] bf16 with page == the mask's Bk;
+    page_table int32 [B,max_pages] (logical key block -> physical page)."""
+    for t in (q, k_pages, v_pages):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q, k_pages, v_pages must be contiguous bf16 CUDA tensors")
+    if page_table.dtype != torch.int32 or not page_table.is_contiguous() or page_table.dim() != 2:
+        raise ValueError("page_table must be contiguous int32 [B, max_pages]")
+    B, Hq, Q_LEN, d = q.shape
+    P, Hkv, page, _ = k_pages.shape
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Q_LEN), dtype=torch.float32, device=q.device)
+    _check(load().fa_flex_forward_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), P, page,
+                                        page_table.shape[1], ctypes.byref(block_mask.c),
+                                        ctypes.byref(score) if score else None, float(scale) if scale else 0.0,
+                                        _ptr(out), _out_code(out), _ptr(lse), B, Hq, Hkv, Q_LEN, KV_LEN, d,
+                                        _ptr(status), _stream(q.device)), "fa_flex_forward_paged")
     return out, lse
 
 

@@ -150,6 +150,28 @@ FA_API fa_status fa_create_block_mask(const fa_mask_rule* rule, int32_t B, int32
                                int32_t Bq, int32_t Bk, void* dev_buf, size_t buf_bytes, fa_block_mask* out,
                                fa_stream_t stream);
 
+/* Prebuilt table, sliced per decode step ("5.1.2 FlexAttention ...", section 5.2; "FlexAttention:
+ * compiler optimisation ...", section 6): from a mask built once for the longest context in global
+ * positions (src->rule.q_offset == NULL), take for each request b the query block row that holds its
+ * token's position q_pos[b] and emit a one-row-per-request mask for fa_flex_decode: Bm = Bz, Hm =
+ * src->Hm, q_len = nq = Bq = 1, the same kv_len / Bk / nk, and the rule of src with q_offset = q_pos
+ * (batch_dependent = 1). A block that is full or empty for the whole block row is so for each of its
+ * rows; only the row's partial blocks are evaluated again, at the one position, as the slice must match
+ * the actual query length. The tables are then exactly those fa_create_block_mask builds for one query
+ * at q_pos[b] (lists, classes and the one-row transpose), at the cost of the partial blocks only.
+ *   src          host pointer to a mask from fa_create_block_mask; src->Bm is 1 or Bz
+ *   dev_q_pos    device int32 [Bz], global query positions; must stay valid while *out is used
+ *   dev_buf      device buffer of >= fa_block_mask_select_bytes(src, Bz) bytes, 256-byte aligned
+ *   out          host struct, filled with pointers into dev_buf (and src's document run arrays)
+ *   dev_status   device int32 or NULL: a position outside [0, src->q_len) sets FA_ERR_DEVICE_CHECK
+ *                and that request's row is empty
+ * Returns FA_ERR_INVALID_ARG (NULL pointers, src with a query offset), FA_ERR_SHAPE (src->Bm or the
+ * document batch not 1 or Bz), FA_ERR_BUFFER_TOO_SMALL. */
+FA_API size_t fa_block_mask_select_bytes(const fa_block_mask* src, int32_t Bz);
+FA_API fa_status fa_block_mask_select_rows(const fa_block_mask* src, const int32_t* dev_q_pos, int32_t Bz,
+                                           void* dev_buf, size_t buf_bytes, fa_block_mask* out,
+                                           int32_t* dev_status, fa_stream_t stream);
+
 /* Element type of O. The softmax statistics and the accumulator are fp32 in every case; FA_OUT_F32
  * stores the fp32 result as is, FA_OUT_BF16 rounds it to bf16 (round to nearest even) on the store. */
 typedef enum { FA_OUT_BF16 = 0, FA_OUT_F32 = 1 } fa_out_dtype;
@@ -176,6 +198,27 @@ FA_API fa_status fa_flex_forward(const void* q, const void* k, const void* v, co
                                  const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype,
                                  float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN,
                                  int32_t d, int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream);
+
+/* The same forward with K and V in a paged cache ("5.1.2 FlexAttention ...", section 5, the paragraph on
+ * turning the logical BlockMask into physical pages; "FlexAttention: compiler optimisation ...", section
+ * 6): the rules stay in logical positions (the mask, causal / window bounds, the score rule and the query
+ * offset all see token positions), and only the K / V fetch of logical key block c of batch row b goes to
+ * physical page page_table[b * max_pages + c]. Several rows may name the same page (a shared prefix).
+ *   k_pages, v_pages  device bf16 [n_pages_total, Hkv, page, d], page == the mask's Bk (one page per key
+ *                     block), 16-byte aligned
+ *   page_table        device int32 [B, max_pages], max_pages >= the mask's nk; entries of blocks the mask
+ *                     never lists are not read. Slots of a page past KV_LEN must hold finite values (they
+ *                     are masked, so any finite value gives the same result).
+ *   other arguments   as fa_flex_forward (no counters)
+ * Returns FA_ERR_SHAPE (page != Bk, max_pages < nk, n_pages_total < 1), FA_ERR_INVALID_ARG (NULL table,
+ * misaligned pointers), and the errors of fa_flex_forward. A listed page id outside [0, n_pages_total)
+ * sets *dev_status = FA_ERR_DEVICE_CHECK (page 0 is read in its place; the output is then not valid). */
+FA_API fa_status fa_flex_forward_paged(const void* q, const void* k_pages, const void* v_pages,
+                                       const int32_t* page_table, int32_t n_pages_total, int32_t page,
+                                       int32_t max_pages, const fa_block_mask* block_mask,
+                                       const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype,
+                                       float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN,
+                                       int32_t KV_LEN, int32_t d, int32_t* dev_status, fa_stream_t stream);
 
 /* Same as fa_flex_forward but always uses the mma.sync kernel (a second, independent kernel over the
  * same tables; used to cross-check the tcgen05 path). */

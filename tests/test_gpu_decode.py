@@ -85,3 +85,62 @@ def test_bad_page_id_reported():
     table[1, 0] = dec.n_pages_total + 5                      # out of range: reported, page skipped
     _, _, st, _ = run_decode(dec, table)
     assert st == fa.ERR_DEVICE_CHECK
+
+
+@pytest.mark.parametrize("page,bq,kind", [(128, 128, "causal"), (64, 128, "window"), (32, 64, "prefix"),
+                                          (128, 16, "window"), (64, 128, "doc")])
+def test_prebuilt_mask_sliced_per_step(page, bq, kind):
+    # the table is built once for the longest context in global positions; each step takes, per request,
+    # the query-block row that holds the request's position and re-evaluates that row's partial blocks at
+    # the position: the result must equal the one-row table built directly, and the decode over it the
+    # oracle
+    prefix = 40 if kind == "prefix" else 0
+    dec = workloads.cfg5(Bz=6, Hq=8, Hkv=2, d=128, page=page, lo=max(1, prefix), hi=9 * page + 5, prefix=prefix)
+    if kind == "window":
+        dec.rule = [("causal",), ("window", 3 * page + 7), ("and",)]
+    dev = "cuda"
+    L = dec.kv_len
+    doc = None
+    if kind == "doc":
+        dec.rule = [("causal",), ("doc",), ("and",)]
+        ids = np.repeat(np.arange(L // 50 + 1, dtype=np.int32), 50)[:L][None, :]
+        doc = torch.from_numpy(ids).to(dev)
+    dec.generate()
+    big = fa.create_block_mask(fa.make_mask_rule(dec.rule, doc_ids=doc), 1, dec.Hq, L, L, bq, page, keep=[doc])
+    qpos = torch.from_numpy(dec.q_offset).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sel = fa.select_rows(big, qpos, status=status)
+    assert sel.shape == (dec.Bz, 1, 1, dec.max_pages)
+    direct = fa.create_block_mask(fa.make_mask_rule(dec.rule, doc_ids=doc, q_offset=qpos, batch_dependent=True),
+                                  dec.Bz, dec.Hq, 1, L, 1, page, keep=[doc, qpos])
+    ts, td = gc.tables_np(sel), gc.tables_np(direct)
+    for name in ("kv_num", "kv_idx", "full_kv_num", "full_kv_idx", "block_class", "q_num", "q_idx", "full_q_num",
+                 "full_q_idx"):
+        assert np.array_equal(ts[name], td[name]), name
+    q = workloads.bf16_torch(dec.q_bits, dev)
+    kp = workloads.bf16_torch(dec.k_bits, dev)
+    vp = workloads.bf16_torch(dec.v_bits, dev)
+    pt = torch.from_numpy(dec.page_table).to(dev)
+    out, lse = fa.flex_decode(q, kp, vp, pt, sel, None, dec.scale, status=status, out_dtype=torch.float32)
+    assert fa.check_status(status) == fa.OK
+    q64, k64, v64 = (synth.bf16_bits_to_f64(x) for x in (dec.q_bits, dec.k_bits, dec.v_bits))
+    o_ref, lse_ref = orc.decode_attention(q64, k64, v64, dec.page_table, dec.kv_lens, dec.rule, dec.scale, None,
+                                          doc_ids=ids if kind == "doc" else None, requests=list(range(dec.Bz)),
+                                          kv_len_table=L)
+    gc.compare(out.cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"prebuilt {kind} page={page} bq={bq}")
+
+
+def test_prebuilt_mask_position_out_of_range():
+    dec = workloads.cfg5(Bz=3, Hq=4, Hkv=2, d=64, page=64, lo=1, hi=5 * 64)
+    dec.generate()
+    L = dec.kv_len
+    big = fa.create_block_mask(fa.make_mask_rule(dec.rule), 1, dec.Hq, L, L, 128, 64)
+    qpos = torch.tensor([5, L + 300, -2], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sel = fa.select_rows(big, qpos, status=status)
+    assert fa.check_status(status) == fa.ERR_DEVICE_CHECK
+    ts = gc.tables_np(sel)
+    assert ts["kv_num"][1:, 0, 0].tolist() == [0, 0] and ts["full_kv_num"][1:, 0, 0].tolist() == [0, 0]
+    # position 5 under causal: key block 0 partial (keys 0..5 of 0..63), nothing else
+    assert ts["kv_num"][0, 0, 0] == 1 and ts["kv_idx"][0, 0, 0, 0] == 0 and ts["full_kv_num"][0, 0, 0] == 0
+    assert not ts["block_class"][1:].any()
