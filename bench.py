@@ -38,6 +38,7 @@ def parse():
                    help="time only the paged decode and print its object as the line (profiling aid)")
     p.add_argument("--decode-requests", type=int, default=64, help="requests in the decode batch")
     p.add_argument("--no-backward", action="store_true")
+    p.add_argument("--no-paged", action="store_true")
     p.add_argument("--backward-only", action="store_true",
                    help="after the forward, time only the backward and print its object as the line (profiling aid)")
     return p.parse_args()
@@ -347,6 +348,11 @@ def ours(args, rank, world, local_rank):
                 print(json.dumps(bwd_line), flush=True)
             return
 
+    # ---------------- paged prefill: the same forward with K/V behind a page table
+    paged_line = None
+    if not args.no_paged:
+        paged_line = bench_paged_prefill(args, dev, pk, w, q, bm, sc, phys_flops)
+
     # ---------------- decode (secondary metric of the same hot path): paged split-KV, 64 requests
     dec_line = None
     if not args.no_decode:
@@ -389,6 +395,8 @@ def ours(args, rank, world, local_rank):
         line["decode"] = dec_line
     if bwd_line:
         line["backward"] = bwd_line
+    if paged_line:
+        line["paged_prefill"] = paged_line
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -434,6 +442,49 @@ def bench_backward(args, dev, pk, w, q, k, v, bm, sc, out, lse, phys_flops):
             "status": fa.status_string(fa.check_status(status))}
 
 
+def time_events(fn, n, stream):
+    """Median milliseconds of fn() over n launches, CUDA events on `stream` after 3 warm-up calls."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def bench_paged_prefill(args, dev, pk, w, q, bm, sc, phys_flops):
+    """fa_flex_forward_paged on the workload's own mask: K and V split into 128-token pages stored at
+    shuffled physical ids (one page per key block), against the contiguous forward timed the same way."""
+    import torch
+
+    from block_sparse_masked_create_gb300 import fa, workloads
+    kpb, table = workloads.paged_kv(w.k_bits, 128, w.seed)
+    vpb, _ = workloads.paged_kv(w.v_bits, 128, w.seed)
+    kp = workloads.bf16_torch(kpb, dev)
+    vp = workloads.bf16_torch(vpb, dev)
+    pt = torch.from_numpy(table).to(dev)
+    k = workloads.bf16_torch(w.k_bits, dev)
+    v = workloads.bf16_torch(w.v_bits, dev)
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n = max(5, args.steps)
+    ms_p = time_events(lambda: fa.flex_forward_paged(q, kp, vp, pt, bm, w.kv_len, sc, w.scale, out=out, lse=lse,
+                                                     status=status), n, stream)
+    ms_c = time_events(lambda: fa.flex_forward(q, k, v, bm, sc, w.scale, out=out, lse=lse, status=status), n, stream)
+    tf = phys_flops / (ms_p * 1e-3) / 1e12
+    return {"workload": f"{w.name} with K/V in 128-token pages at shuffled physical ids ({kpb.shape[0]} pages)",
+            "ms_median": ms_p, "tflops": tf, "pct_bf16_peak": tf / pk["bf16"],
+            "contiguous_ms_median": ms_c, "paged_over_contiguous": ms_p / ms_c,
+            "status": fa.status_string(fa.check_status(status))}
+
+
 def bench_decode(args, dev, pk):
     import numpy as np
     import torch
@@ -463,12 +514,20 @@ def bench_decode(args, dev, pk):
         b.record(stream)
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in evs]
+    # per-step decode table: a fresh one-row build vs the row selection from a table prebuilt once for the
+    # longest context (global positions, 128-row query blocks)
+    L = d.kv_len
+    big = fa.create_block_mask(fa.make_mask_rule(d.rule), 1, d.Hq, L, L, 128, d.page, device=dev)
+    sel = fa.select_rows(big, off)
+    ms_build = time_events(lambda: fa.recreate_block_mask(bm, rule, d.Bz, d.Hq, 1, d.kv_len, 1, d.page), n, stream)
+    ms_sel = time_events(lambda: fa.select_rows(big, off, out=sel), n, stream)
     kv_bytes = int(sum(int(L) for L in d.kv_lens)) * d.Hkv * d.d * 2 * 2
     other = q.numel() * 2 + out.numel() * 2 + lse.numel() * 4 + pt.numel() * 4
     med = statistics.median(ms)
     gbs = (kv_bytes + other) / (med * 1e-3) / 1e9
     return {"workload": f"cfg5 paged decode: {d.Bz} requests, Hq=32, Hkv=8, d=128, 128-token pages, L~U[1024,32768]",
             "kv_gb": kv_bytes / 1e9, "ms_median": med, "GB/s": gbs, "pct_hbm": gbs / pk["hbm"],
+            "step_mask_build_us": 1e3 * ms_build, "step_mask_from_prebuilt_us": 1e3 * ms_sel,
             "status": fa.status_string(fa.check_status(status)),
             "note": "KV read once per KV head; K/V pages 2x%.1f GB > L2" % (d.k_bits.nbytes / 1e9)}
 

@@ -184,6 +184,20 @@ def cfg5(Bz: int = 64, Hq: int = 32, Hkv: int = 8, d: int = 128, page: int = 128
                   max_pages, lens, table, ptot, rule, {}, 1.0 / math.sqrt(d), seed)
 
 
+def paged_kv(bits: np.ndarray, page: int, seed: int):
+    """Contiguous K or V bits [B, Hkv, N, d] -> pages [B * ceil(N / page), Hkv, page, d] at seeded shuffled
+    physical ids, and the page table int32 [B, ceil(N / page)] (slots past N hold zeros)."""
+    B, Hkv, N, d = bits.shape
+    npg = -(-N // page)
+    perm = synth.permutation(seed, TID_PERM, B * npg).astype(np.int32)
+    padded = np.zeros((B, Hkv, npg * page, d), dtype=bits.dtype)
+    padded[:, :, :N] = bits
+    logical = padded.reshape(B, Hkv, npg, page, d).transpose(0, 2, 1, 3, 4).reshape(B * npg, Hkv, page, d)
+    pages = np.empty_like(logical)
+    pages[perm] = logical
+    return pages, perm.reshape(B, npg)
+
+
 def bf16_torch(bits: np.ndarray, device=None):
     """uint16 bf16 bit patterns -> torch.bfloat16 tensor (a byte-for-byte view, no rounding)."""
     import torch
