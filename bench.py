@@ -436,7 +436,7 @@ def bench_backward(args, dev, pk, w, q, k, v, bm, sc, out, lse, phys_flops):
     flop = 2.5 * phys_flops
     tf = flop / (med * 1e-3) / 1e12
     return {"workload": f"{w.name} backward: dout ~ N(0,1) bf16, dq/dk/dv fp32",
-            "kernels": "delta + dQ (row lists) + dK/dV (query-side transpose), mma.sync m16n8k16",
+            "kernels": "delta + dQ (row lists) + dK/dV (query-side transpose); tcgen05 for 128x128 blocks",
             "ms_median": med, "algorithmic_tflop": flop / 1e12, "tflops": tf, "pct_bf16_peak": tf / pk["bf16"],
             "peak_src": f"{pk['src']} bf16 burst", "launches_per_step": 3,
             "status": fa.status_string(fa.check_status(status))}

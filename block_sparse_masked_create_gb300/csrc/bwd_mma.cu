@@ -421,6 +421,9 @@ cudaError_t launch_backward(const BwdArgs& a, cudaStream_t st) {
   bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  const int t = launch_bwd_tc5(a, st);
+  if (t == FA_OK) return cudaSuccess;
+  if (t != FA_ERR_UNSUPPORTED) return cudaErrorLaunchFailure;
   if (a.d == 64) return launch_d<64>(a, st);
   if (a.d == 128) return launch_d<128>(a, st);
   return cudaErrorInvalidValue;

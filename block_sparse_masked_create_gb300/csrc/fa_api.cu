@@ -330,6 +330,7 @@ static int backward_impl(const void* q, const void* k, const void* v, const void
   a.score = make_score(score, KV_LEN);
   a.mask = dev_mask(bm);
   a.status = dev_status;
+  a.timeout_ns = g_timeout_ns.load();
   if ((long long)B * Hq > 65535LL * 65535LL || Hq > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
   return launch_backward(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

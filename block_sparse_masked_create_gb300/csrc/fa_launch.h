@@ -113,9 +113,12 @@ struct BwdArgs {
   DevScore score;
   DevMask mask;
   int32_t* status;
+  uint64_t timeout_ns;  // bound of every in-kernel wait (tcgen05 kernels)
 };
 
 cudaError_t launch_backward(const BwdArgs& a, cudaStream_t st);
+// dQ and dK/dV on tcgen05 for 128 x 128 blocks; FA_OK / FA_ERR_UNSUPPORTED / FA_ERR_CUDA
+int launch_bwd_tc5(const BwdArgs& a, cudaStream_t st);
 
 cudaError_t launch_debug_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t st);
 

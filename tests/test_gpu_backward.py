@@ -66,6 +66,11 @@ DOCS = np.repeat(np.arange(6, dtype=np.int32), [70, 30, 100, 20, 60, 40])[None, 
     ("dense_64x128", 1, 2, 1, 192, 256, 64, 64, 128, [("true",)], None),
     ("prefix_or_causal_128x64", 1, 2, 2, 256, 256, 128, 128, 64, [("causal",), ("prefix", 40), ("or",)], None),
     ("ragged", 1, 2, 2, 200, 200, 128, 128, 128, [("causal",)], None),
+    ("causal_d64_128x128", 1, 2, 1, 384, 384, 64, 128, 128, [("causal",)], None),
+    ("window_gqa_ragged_128", 2, 4, 1, 300, 300, 128, 128, 128, CW(150), None),
+    ("dense_rect_128", 1, 2, 2, 192, 320, 128, 128, 128, [("true",)], None),
+    ("prefix_or_window_softcap_d64_128", 1, 2, 2, 400, 400, 64, 128, 128,
+     [("causal",), ("window", 90), ("and",), ("prefix", 30), ("or",)], {"softcap": 30.0}),
 ])
 def test_backward_small(cfg):
     name, B, Hq, Hkv, ql, kl, d, bq, bk, rule, score = cfg
@@ -90,11 +95,24 @@ def test_backward_unseen_keys_have_zero_gradient():
     assert np.abs(dk[:, :, 64:]).max() == 0.0 and np.abs(dv[:, :, 64:]).max() == 0.0
 
 
-def test_backward_empty_rows_give_zero():
+@pytest.mark.parametrize("blk", [64, 128])
+def test_backward_empty_rows_give_zero(blk):
     # no pair allowed at all: every row is empty (O = 0, LSE = -inf) and every gradient is exactly zero
-    w = case("all_empty", 1, 2, 1, 130, 130, 64, 64, 64, [("prefix", 0)])
+    w = case("all_empty", 1, 2, 1, 130, 130, 64, blk, blk, [("prefix", 0)])
     dq, dk, dv = run_backward(w)
     assert np.abs(dq).max() == 0.0 and np.abs(dk).max() == 0.0 and np.abs(dv).max() == 0.0
+
+
+def test_backward_unseen_key_blocks_128():
+    # 128x128 blocks: key blocks 1 and 2 are never visited (causal and a 128-key prefix), so their CTAs
+    # have no query block to walk and write zero dK, dV
+    w = case("unseen_blocks", 1, 2, 1, 384, 384, 128, 128, 128, [("causal",), ("prefix", 128), ("and",)])
+    dq, dk, dv = run_backward(w)
+    want = oracle_grads(w)
+    for g, r in zip((dq, dk, dv), want):
+        G = max(float(np.abs(r).max()), 1e-6)
+        assert np.abs(g - r).max() <= G_MAX * G
+    assert np.abs(dk[:, :, 128:]).max() == 0.0 and np.abs(dv[:, :, 128:]).max() == 0.0
 
 
 def test_backward_cfg2_shape_sampled_heads():
