@@ -42,11 +42,14 @@ struct BwdTc5 {
   static constexpr int kKvOffStat = 6 * kTile;  // float [2][3][128]: LSE*log2e, D, query document ids
   static constexpr int kKvOffBar = kKvOffStat + 2 * 3 * 128 * 4;
   static constexpr int kKvSmem = kKvOffBar + 256;
-  // dQ kernel shared memory: Q, dO, two stages of (K, V), key document ids [2][128], barriers
-  static constexpr int kQOffQ = 0, kQOffDO = kTile, kQOffStage = 2 * kTile;
-  static constexpr int kQOffDoc = 6 * kTile;
+  // dQ kernel shared memory: Q, dO, a 3-slot K ring (K(k) is read by S(k) and, last, by dQ(k); the
+  // third slot lets K(k+1) arrive while dQ(k-1) still reads its slot), a 2-slot V ring (V(k) is read by
+  // dP(k) only), key document ids [2][128], barriers
+  static constexpr int kQOffQ = 0, kQOffDO = kTile, kQOffK = 2 * kTile, kQOffV = 5 * kTile;
+  static constexpr int kQOffDoc = 7 * kTile;
   static constexpr int kQOffBar = kQOffDoc + 2 * 128 * 4;
   static constexpr int kQSmem = kQOffBar + 256;
+  static_assert(kKvSmem <= 232448 && kQSmem <= 232448, "shared memory per CTA");
 };
 
 // K-major operand tile (TMA box {64, 128} with the 128-byte swizzle): k-step ks (16 elements) starts at
@@ -315,30 +318,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int doc_j = a.rule.any_doc ? doc_at(a.rule, b, j) : -1;
     const float sl2 = a.scale * kLog2e;
     const float ain = a.scale * a.score.inv_softcap, aout = a.score.softcap * kLog2e;
+    // Per-query statistics of an item, one value per thread: LSE * log2(e) (+inf past the sequence or
+    // for an empty row, so P = 0 there) in threads 0-127, D and the query row's document id in threads
+    // 128-255. Item k + 1's are loaded into registers at the start of item k and stored to the shared
+    // buffer (k + 1) & 1 at its end, so their latency hides behind item k; the barrier at the top of each
+    // item publishes them, and the buffer they overwrite was last read before the previous barrier.
+    int h_n = 0, r_n = 0;
+    bool p_n = false;
+    float v_n = 0.f;
+    int doc_n = -1;
+    auto fetch = [&](int kk) {
+      kv_item(a, b, hk, c, kk, h_n, r_n, p_n);
+      const int64_t i = (int64_t)r_n * 128 + (tid & 127);
+      const size_t qrow = ((size_t)b * a.Hq + h_n) * a.q_len + i;
+      const bool in = i < a.q_len;
+      v_n = tid < 128 ? (in ? __ldg(a.lse + qrow) : -INFINITY) : (in ? __ldg(a.delta + qrow) : 0.f);
+      if (a.rule.any_doc && tid >= 128) doc_n = doc_at(a.rule, b, i + off);
+    };
+    auto publish = [&](int kk) {
+      float* st = sStat + (kk & 1) * 384;
+      const int x = tid & 127;
+      if (tid < 128) {
+        st[x] = v_n == -INFINITY ? INFINITY : v_n * kLog2e;
+      } else {
+        st[128 + x] = v_n;
+        if (a.rule.any_doc) reinterpret_cast<int*>(st)[256 + x] = doc_n;
+      }
+    };
+    if (n > 0) {
+      fetch(0);
+      publish(0);
+    }
     bool ok = true;  // warp-uniform; made CTA-uniform among the gradient warps at each item's barrier
     for (int k = 0; k < n; ++k) {
-      int h, r;
-      bool partial;
-      kv_item(a, b, hk, c, k, h, r, partial);
-      // this item's per-query statistics: LSE * log2(e) (+inf past the sequence or for an empty row, so
-      // P = 0 there), D, and the query rows' document ids
-      float* st_l = sStat + (k & 1) * 384;
-      {
-        const int x = tid & 127;
-        const int64_t i = (int64_t)r * 128 + x;
-        const size_t qrow = ((size_t)b * a.Hq + h) * a.q_len + i;
-        if (tid < 128) {
-          float l = i < a.q_len ? __ldg(a.lse + qrow) : -INFINITY;
-          st_l[x] = l == -INFINITY ? INFINITY : l * kLog2e;
-        } else {
-          st_l[128 + x] = i < a.q_len ? __ldg(a.delta + qrow) : 0.f;
-          if (a.rule.any_doc) reinterpret_cast<int*>(st_l)[256 + x] = doc_at(a.rule, b, i + off);
-        }
-      }
       if (grad_bar_any(!ok)) {
         ok = false;
         break;
       }
+      const int h = h_n, r = r_n;
+      const bool partial = p_n;
+      float* st_l = sStat + (k & 1) * 384;
+      if (k + 1 < n) fetch(k + 1);
       const float slope = (SK == SK_ALIBI || SK == SK_GENERIC) && a.score.alibi ? __ldg(a.score.alibi + h) : 0.f;
       // ALiBi (log2 domain): -slope log2e (i_g - j), i_g - j = d0 + column; base at this warpgroup's first
       const int64_t d0 = (int64_t)r * 128 + off - j;
@@ -398,11 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- dS^T = P g (dP^T - D), written over dP^T as bf16 pairs
       if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_dp, (uint32_t)(k & 1), wc)))) continue;
       tc5_fence_after();
+      uint32_t dv2[2][32];
+      tc5_ld32(lane_addr + C::kKvColDP + 64 * wg, dv2[0]);
+      tc5_ld32(lane_addr + C::kKvColDP + 64 * wg + 32, dv2[1]);
+      tc5_wait_ld();
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t dv[32];
-        tc5_ld32(lane_addr + C::kKvColDP + 64 * wg + 32 * half, dv);
-        tc5_wait_ld();
+        const uint32_t (&dv)[32] = dv2[half];
         uint32_t pk[16];
         const float4* dl4 = reinterpret_cast<const float4*>(st_l + 128 + 64 * wg + 32 * half);
 #pragma unroll
@@ -418,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc5_wait_st();
       tc5_fence_before();
       mbar_arrive(bar_ds);
+      if (k + 1 < n) publish(k + 1);
     }
     // ---- epilogue: dV and scale * dK of this key row, fp32 (rows past kv_len are not written)
     // (tcgen05.ld is warp-collective: every lane loads, only rows inside the sequence store)
@@ -490,24 +513,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* sDoc = reinterpret_cast<int*>(smem + C::kQOffDoc);  // [2][128] key document ids
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kQOffBar);
   uint64_t* bar_qdo = bars + 0;
-  uint64_t* bar_full = bars + 1;   // [2]
-  uint64_t* bar_empty = bars + 3;  // [2]
-  uint64_t* bar_s = bars + 5;      // [2]
-  uint64_t* bar_dp = bars + 7;
-  uint64_t* bar_ds = bars + 8;
-  uint64_t* bar_done = bars + 9;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 10);
-  volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(bars + 11);
-  auto stageK = [&](int st) { return smem + C::kQOffStage + st * 2 * C::kTile; };
-  auto stageV = [&](int st) { return smem + C::kQOffStage + st * 2 * C::kTile + C::kTile; };
+  uint64_t* bar_kfull = bars + 1;   // [3]
+  uint64_t* bar_kempty = bars + 4;  // [3]
+  uint64_t* bar_vfull = bars + 7;   // [2]
+  uint64_t* bar_vempty = bars + 9;  // [2]
+  uint64_t* bar_s = bars + 11;      // [2] S buffers
+  uint64_t* bar_dp = bars + 13;
+  uint64_t* bar_ds = bars + 14;
+  uint64_t* bar_done = bars + 15;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(bars + 17);
+  auto slotK = [&](int k) { return smem + C::kQOffK + (k % 3) * C::kTile; };
+  auto slotV = [&](int k) { return smem + C::kQOffV + (k & 1) * C::kTile; };
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
       *s_abort = 0;
       mbar_init(bar_qdo, 1);
+      for (int i = 0; i < 3; ++i) {
+        mbar_init(bar_kfull + i, 1);
+        mbar_init(bar_kempty + i, 1);
+      }
       for (int i = 0; i < 2; ++i) {
-        mbar_init(bar_full + i, 1);
-        mbar_init(bar_empty + i, 1);
+        mbar_init(bar_vfull + i, 1);
+        mbar_init(bar_vempty + i, 1);
         mbar_init(bar_s + i, 1);
       }
       mbar_init(bar_dp, 1);
@@ -541,22 +570,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------------ TMA producer: K, V per block
-    int issued[2] = {0, 0};
+    int issuedK[3] = {0, 0, 0}, issuedV[2] = {0, 0};
     for (int k = 0; k < n; ++k) {
-      const int st = k & 1;
-      if (k >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(bar_empty + st, (uint32_t)(((k >> 1) - 1) & 1), wc))) break;
       const int c = item_col(k);
-      mbar_arrive_expect_tx_elect(bar_full + st, 2 * C::kTile);
+      const int sk = k % 3, sv = k & 1;
+      if (k >= 3 && !__all_sync(0xFFFFFFFFu, mbar_wait(bar_kempty + sk, (uint32_t)((k / 3 - 1) & 1), wc))) break;
+      mbar_arrive_expect_tx_elect(bar_kfull + sk, C::kTile);
 #pragma unroll
-      for (int x = 0; x < D / 64; ++x) {
-        tma_load_3d_elect(stageK(st) + x * 16384, &tmK, x * 64, c * 128, b * a.Hkv + hk, bar_full + st);
-        tma_load_3d_elect(stageV(st) + x * 16384, &tmV, x * 64, c * 128, b * a.Hkv + hk, bar_full + st);
-      }
-      issued[st] = (k >> 1) + 1;
+      for (int x = 0; x < D / 64; ++x)
+        tma_load_3d_elect(slotK(k) + x * 16384, &tmK, x * 64, c * 128, b * a.Hkv + hk, bar_kfull + sk);
+      issuedK[sk] = k / 3 + 1;
+      if (k >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(bar_vempty + sv, (uint32_t)(((k >> 1) - 1) & 1), wc))) break;
+      mbar_arrive_expect_tx_elect(bar_vfull + sv, C::kTile);
+#pragma unroll
+      for (int x = 0; x < D / 64; ++x)
+        tma_load_3d_elect(slotV(k) + x * 16384, &tmV, x * 64, c * 128, b * a.Hkv + hk, bar_vfull + sv);
+      issuedV[sv] = (k >> 1) + 1;
     }
     if (n > 0) mbar_wait_drain(bar_qdo, 0, a.timeout_ns);
-    for (int st = 0; st < 2; ++st)
-      if (issued[st] > 0) mbar_wait_drain(bar_full + st, (uint32_t)((issued[st] - 1) & 1), a.timeout_ns);
+    for (int i = 0; i < 3; ++i)
+      if (issuedK[i] > 0) mbar_wait_drain(bar_kfull + i, (uint32_t)((issuedK[i] - 1) & 1), a.timeout_ns);
+    for (int i = 0; i < 2; ++i)
+      if (issuedV[i] > 0) mbar_wait_drain(bar_vfull + i, (uint32_t)((issuedV[i] - 1) & 1), a.timeout_ns);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);  // S, dP: N = 128 keys
@@ -564,35 +599,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t dodesc = sdesc_sw128(smem_u32(sDO), 16, 1024);
     bool ok = n > 0 && __all_sync(0xFFFFFFFFu, mbar_wait(bar_qdo, 0, wc));
-    auto issue_s = [&](int k) -> bool {
-      const int st = k & 1;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_full + st, (uint32_t)((k >> 1) & 1), wc))) return false;
+    auto issue_s = [&](int k) -> bool {  // S(k) = Q K(k)^T into S buffer k & 1
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_kfull + k % 3, (uint32_t)((k / 3) & 1), wc))) return false;
       tc5_fence_after();
-      const uint64_t kd = sdesc_sw128(smem_u32(stageK(st)), 16, 1024);
+      const uint64_t kd = sdesc_sw128(smem_u32(slotK(k)), 16, 1024);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        tc5_mma_ss_elect(tmem + C::kQColS0 + 128 * st, qdesc + kmaj_step(ks), kd + kmaj_step(ks), idesc_s,
+        tc5_mma_ss_elect(tmem + C::kQColS0 + 128 * (k & 1), qdesc + kmaj_step(ks), kd + kmaj_step(ks), idesc_s,
                          ks > 0 ? 1u : 0u);
-      tc5_commit_elect(bar_s + st);
+      tc5_commit_elect(bar_s + (k & 1));
       return true;
     };
     if (ok) ok = issue_s(0);
     for (int k = 0; k < n && ok; ++k) {
-      const int st = k & 1;
-      const uint64_t vd = sdesc_sw128(smem_u32(stageV(st)), 16, 1024);
+      if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_vfull + (k & 1), (uint32_t)((k >> 1) & 1), wc)))) break;
+      tc5_fence_after();
+      const uint64_t vd = sdesc_sw128(smem_u32(slotV(k)), 16, 1024);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
         tc5_mma_ss_elect(tmem + C::kQColDP, dodesc + kmaj_step(ks), vd + kmaj_step(ks), idesc_s, ks > 0 ? 1u : 0u);
       tc5_commit_elect(bar_dp);
+      tc5_commit_elect(bar_vempty + (k & 1));
       if (k + 1 < n && !(ok = issue_s(k + 1))) break;  // its buffer held S(k-1), read before dS(k-1)
       if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_ds, (uint32_t)(k & 1), wc)))) break;
       tc5_fence_after();
-      const uint64_t k_mn = sdesc_sw128(smem_u32(stageK(st)), 16384, 1024);
+      const uint64_t k_mn = sdesc_sw128(smem_u32(slotK(k)), 16384, 1024);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
         tc5_mma_ts_elect(tmem + C::kQColDQ, tmem + C::kQColDP + packed_step(ks), k_mn + mnmaj_step(ks), idesc_q,
                          (k > 0 || ks > 0) ? 1u : 0u);
-      tc5_commit_elect(bar_empty + st);
+      tc5_commit_elect(bar_kempty + k % 3);
     }
     tc5_commit_elect(bar_done);
   } else {
@@ -637,11 +673,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s + (k & 1), (uint32_t)((k >> 1) & 1), wc)))) continue;
       tc5_fence_after();
       float pg[64];
+      uint32_t sv2[2][32];
+      tc5_ld32(lane_addr + C::kQColS0 + 128 * (k & 1) + 64 * wg, sv2[0]);
+      tc5_ld32(lane_addr + C::kQColS0 + 128 * (k & 1) + 64 * wg + 32, sv2[1]);
+      tc5_wait_ld();
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t sv[32];
-        tc5_ld32(lane_addr + C::kQColS0 + 128 * (k & 1) + 64 * wg + 32 * half, sv);
-        tc5_wait_ld();
+        const uint32_t (&sv)[32] = sv2[half];
         // ALiBi (log2 domain): -slope log2e (i_g - j) = base_w + slope log2e (column - 64 wg)
         const float base_w = -psl2 * (float)(ig - (j0 + 64 * wg));
 #pragma unroll
@@ -667,11 +705,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_dp, (uint32_t)(k & 1), wc)))) continue;
       tc5_fence_after();
+      uint32_t dv2[2][32];
+      tc5_ld32(lane_addr + C::kQColDP + 64 * wg, dv2[0]);
+      tc5_ld32(lane_addr + C::kQColDP + 64 * wg + 32, dv2[1]);
+      tc5_wait_ld();
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t dv[32];
-        tc5_ld32(lane_addr + C::kQColDP + 64 * wg + 32 * half, dv);
-        tc5_wait_ld();
+        const uint32_t (&dv)[32] = dv2[half];
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2)
