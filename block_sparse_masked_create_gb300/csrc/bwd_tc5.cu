@@ -98,11 +98,15 @@ __device__ __forceinline__ float score_g(const DevScore& sc, int h, float x, int
 
 // Allowed query rows (global positions [ig0, ig0 + w), w <= 128) of one key position j: the rule's terms
 // read with the roles of row and column swapped (causal: i >= j; window: i < j + W; prefix: j < P;
-// document: doc(i) == doc(j), from the rows' ids in `qdoc`).
+// document: doc(i) == doc(j), as the run [run_lo, run_hi) of j's id when `use_run` (ids that never
+// decrease, and an id other than -1, which rows outside the id array also read), else from the rows' ids
+// in `qdoc`).
 __device__ __forceinline__ Bits128 rule_key_bits(const DevRule& R, int64_t j, int64_t ig0, int w, int doc_j,
-                                                 const int* qdoc) {
+                                                 const int* qdoc, bool use_run, int64_t run_lo, int64_t run_hi) {
   Bits128 db = {{0u, 0u, 0u, 0u}};
-  if (R.any_doc) {
+  if (R.any_doc && use_run) {
+    db = range_bits(clamp_rel(run_lo - ig0, w), clamp_rel(run_hi - ig0, w));
+  } else if (R.any_doc) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       uint32_t wd = 0u;
@@ -316,6 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     const int64_t off = a.rule.q_offset ? (int64_t)__ldg(a.rule.q_offset + (a.mask.Bm > 1 ? b : 0)) : 0;
     const int doc_j = a.rule.any_doc ? doc_at(a.rule, b, j) : -1;
+    // document equality of this key as the run of its id (ids that never decrease)
+    const bool runs = a.rule.any_doc && doc_j != -1 && doc_runs_usable(a.rule, b);
+    int64_t run_lo = 0, run_hi = 0;
+    if (runs) doc_run_of(a.rule, b, j, run_lo, run_hi);
     const float sl2 = a.scale * kLog2e;
     const float ain = a.scale * a.score.inv_softcap, aout = a.score.softcap * kLog2e;
     // Per-query statistics of an item, one value per thread: LSE * log2(e) (+inf past the sequence or
@@ -366,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t allowed[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};  // this warpgroup's 64 query columns
       if (partial) {
         const Bits128 bits = rule_key_bits(a.rule, j, (int64_t)r * 128 + off, (int)min((int64_t)128, (int64_t)a.q_len - (int64_t)r * 128),
-                                           doc_j, reinterpret_cast<const int*>(st_l) + 256);
+                                           doc_j, reinterpret_cast<const int*>(st_l) + 256, runs, run_lo, run_hi);
         allowed[0] = bits.w[2 * wg];
         allowed[1] = bits.w[2 * wg + 1];
       }
@@ -647,6 +655,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       dlt = __ldg(a.delta + qrow);
     }
     const int doc_i = a.rule.any_doc ? doc_at(a.rule, b, ig) : -1;
+    // document equality of this row as the run of its id (ids that never decrease; every key position
+    // lies inside the id array)
+    const bool runs = a.rule.any_doc && ig >= 0 && ig < a.rule.doc_len && doc_runs_usable(a.rule, b);
+    int64_t run_lo = 0, run_hi = 0;
+    if (runs) doc_run_of(a.rule, b, ig, run_lo, run_hi);
     const float slope = (SK == SK_ALIBI || SK == SK_GENERIC) && a.score.alibi ? __ldg(a.score.alibi + h) : 0.f;
     const float sl2 = a.scale * kLog2e, psl2 = slope * kLog2e;
     const float ain = a.scale * a.score.inv_softcap, aout = a.score.softcap * kLog2e;
@@ -665,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (partial) {
         const int w = (int)min((int64_t)128, (int64_t)a.kv_len - j0);
         const Bits128 bits = rule_row_bits(a.rule, ig, j0, w, doc_i, [&](int d) {
+          if (runs) return range_bits(clamp_rel(run_lo - j0, w), clamp_rel(run_hi - j0, w));
           return doc_bits<4>(w, d, [&](int cc) { return kdoc[cc]; });
         });
         allowed[0] = bits.w[2 * wg];

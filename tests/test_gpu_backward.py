@@ -119,3 +119,16 @@ def test_backward_cfg2_shape_sampled_heads():
     # the causal workload's block geometry at reduced batch (B=1, 2 heads, N=2048): full oracle gradients
     w = workloads.cfg2(B=1, H=2, n=2048).generate()
     check(w)
+
+
+@pytest.mark.parametrize("kind", ["unsorted", "sorted_with_minus_one"])
+def test_backward_documents_id_orders(kind):
+    # document equality from id runs (ids that never decrease) and from id-by-id comparison (any order;
+    # -1 ids, which positions outside the id array also read), on 128x128 blocks with GQA
+    rng = np.random.default_rng(91 if kind == "unsorted" else 92)
+    n = 384
+    ids = rng.integers(-1 if kind != "unsorted" else 0, 4, size=n).astype(np.int32)
+    if kind != "unsorted":
+        ids = np.sort(ids)
+    w = case(f"doc_{kind}", 1, 4, 2, n, n, 128, 128, 128, [("causal",), ("doc",), ("and",)], None, doc=ids[None, :])
+    check(w)
