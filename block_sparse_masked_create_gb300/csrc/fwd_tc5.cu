@@ -364,15 +364,15 @@ __global__ void __launch_bounds__(Roles<NT>::kThreads, Roles<NT>::kCtasPerSm)
           tc5_commit_elect(&bar_empty[sk]);
         }
         for (int j = 0; j < n && ok; ++j) {
-          if (!(ok = wait_p(0, j))) break;
+          // V(j) and K(j+1) landed long ago: take their slots before waiting for P, so that the wait on
+          // their barriers is off the path from P(j) to the next products
           const int sv = take();
           if (sv < 0) { ok = false; break; }
-          mma_pv(0, sv, j > 0);
           sk = -1;
-          if (j + 1 < n) {
-            if ((sk = take()) < 0) { ok = false; break; }
-            mma_qk(0, sk);
-          }
+          if (j + 1 < n && (sk = take()) < 0) { ok = false; break; }
+          if (!(ok = wait_p(0, j))) break;
+          mma_pv(0, sv, j > 0);
+          if (sk >= 0) mma_qk(0, sk);
           if (!(ok = wait_p(1, j))) break;
           mma_pv(1, sv, j > 0);
           tc5_commit_elect(&bar_empty[sv]);
@@ -397,14 +397,15 @@ __global__ void __launch_bounds__(Roles<NT>::kThreads, Roles<NT>::kCtasPerSm)
           for (int t = 0; t < 2; ++t) {
             const int nt = t ? T1.n : T0.n;
             if (!ok || j >= nt) continue;
-            if (!(ok = wait_p(t, j))) break;
+            // V_t(j) and K_t(j+1): slots taken before the wait for P (see above)
             const int sv = take();
             if (sv < 0) { ok = false; break; }
+            int sk = -1;
+            if (j + 1 < nt && (sk = take()) < 0) { ok = false; break; }
+            if (!(ok = wait_p(t, j))) break;
             mma_pv(t, sv, j > 0);
             tc5_commit_elect(&bar_empty[sv]);
-            if (j + 1 < nt) {
-              const int sk = take();
-              if (sk < 0) { ok = false; break; }
+            if (sk >= 0) {
               mma_qk(t, sk);
               tc5_commit_elect(&bar_empty[sk]);
             }
