@@ -132,3 +132,23 @@ def test_backward_documents_id_orders(kind):
         ids = np.sort(ids)
     w = case(f"doc_{kind}", 1, 4, 2, n, n, 128, 128, 128, [("causal",), ("doc",), ("and",)], None, doc=ids[None, :])
     check(w)
+
+
+def test_backward_cfg2_full_size_sampled_heads():
+    # the benchmarked configuration itself (B=4, H=16, N=4096, d=128, causal), run whole on the GPU; two
+    # seeded (b, h) pairs checked against the oracle on that head alone (one KV head per query head, so a
+    # head is an independent problem)
+    w = workloads.cfg2().generate()
+    dq, dk, dv = run_backward(w)
+    rng = np.random.default_rng(5)
+    pairs = [(0, 0), (int(rng.integers(w.B)), int(rng.integers(w.Hq)))]
+    do = w.dout_bits()
+    for b, h in pairs:
+        f = lambda x: synth.bf16_bits_to_f64(x[b:b + 1, h:h + 1])
+        want = orc.attention_backward(f(w.q_bits), f(w.k_bits), f(w.v_bits), f(do), w.rule, w.scale)
+        for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), want):
+            g = g[b:b + 1, h:h + 1]
+            G = max(float(np.abs(r).max()), 1e-6)
+            err = np.abs(g - r)
+            assert err.max() <= G_MAX * G, f"({b},{h}) {name}: max err {err.max():.3e} > {G_MAX} x {G:.3e}"
+            assert err.mean() <= G_MEAN * G, f"({b},{h}) {name}: mean err {err.mean():.3e}"

@@ -155,3 +155,16 @@ def test_page_size_must_match_the_key_block():
     with pytest.raises(fa.FaError) as e:
         run_paged(w, kp, vp, table)
     assert e.value.code == fa.ERR_SHAPE
+
+
+def test_paged_cfg2_full_size_equals_contiguous():
+    # the benchmarked configuration with K/V in 128-token pages at shuffled ids (the bench's paged line):
+    # bit-identical to the contiguous forward
+    w = workloads.cfg2().generate()
+    kpb, table = workloads.paged_kv(w.k_bits, 128, w.seed)
+    vpb, _ = workloads.paged_kv(w.v_bits, 128, w.seed)
+    o_p, lse_p, st, _keep = run_paged(w, kpb, vpb, table)
+    assert st == fa.OK
+    r = gc.run_prefill(w, out_dtype=torch.float32)
+    assert np.array_equal(o_p.view(np.uint32), r["out"].cpu().numpy().view(np.uint32))
+    assert np.array_equal(lse_p.view(np.uint32), r["lse"].cpu().numpy().view(np.uint32))
