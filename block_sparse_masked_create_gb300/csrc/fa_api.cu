@@ -549,6 +549,156 @@ fa_status fa_flex_forward_paged(const void* q, const void* k_pages, const void* 
                                  PagedKV{page_table, n_pages_total, page, max_pages});
 }
 
+// ------------------------------------------------------------------------------------------------
+// Forward from host buffers: chunks of KV heads of one batch row stream through two device slots; the
+// copies in, the kernels (two streams, so a chunk's CTAs can fill the SMs the previous chunk's short CTAs
+// free) and the copies out run on separate streams, so each chunk's copies overlap its neighbours' work.
+// ------------------------------------------------------------------------------------------------
+struct HostPlan {
+  int ck, g, n_chunks, chunks_per_b;
+  size_t q_bytes, kv_bytes, o_bytes, l_bytes, slot_bytes;
+};
+
+static int host_plan(int B, int Hq, int Hkv, int Q_LEN, int KV_LEN, int d, int out_dtype, HostPlan* P) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Q_LEN < 1 || KV_LEN < 1 || Hq % Hkv) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (out_dtype != FA_OUT_BF16 && out_dtype != FA_OUT_F32) return FA_ERR_INVALID_ARG;
+  P->g = Hq / Hkv;
+  // about eight chunks per call (enough to overlap), never more than one batch row per chunk
+  const int units = B * Hkv;
+  P->ck = std::max(1, std::min(Hkv, units / 8));
+  P->chunks_per_b = (Hkv + P->ck - 1) / P->ck;
+  P->n_chunks = B * P->chunks_per_b;
+  const size_t qh = (size_t)Q_LEN * d, kh = (size_t)KV_LEN * d;
+  P->q_bytes = align256((size_t)P->ck * P->g * qh * 2);
+  P->kv_bytes = align256((size_t)P->ck * kh * 2);
+  P->o_bytes = align256((size_t)P->ck * P->g * qh * (out_dtype == FA_OUT_F32 ? 4 : 2));
+  P->l_bytes = align256((size_t)P->ck * P->g * Q_LEN * 4);
+  P->slot_bytes = P->q_bytes + 2 * P->kv_bytes + P->o_bytes + P->l_bytes;
+  return FA_OK;
+}
+
+size_t fa_forward_host_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d,
+                                       int32_t out_dtype) {
+  HostPlan P;
+  return host_plan(B, Hq, Hkv, Q_LEN, KV_LEN, d, out_dtype, &P) == FA_OK ? 2 * P.slot_bytes : 0;
+}
+
+fa_status fa_flex_forward_host(const void* host_q, const void* host_k, const void* host_v,
+                               const fa_block_mask* block_mask, const fa_score_rule* score_rule, float scale,
+                               void* host_out, int32_t out_dtype, float* host_lse, int32_t B, int32_t Hq, int32_t Hkv,
+                               int32_t Q_LEN, int32_t KV_LEN, int32_t d, void* dev_workspace, size_t workspace_bytes,
+                               int32_t* dev_status, fa_stream_t stream) {
+  if (!host_q || !host_k || !host_v || !block_mask || !host_out || !host_lse || !dev_workspace)
+    return FA_ERR_INVALID_ARG;
+  HostPlan P;
+  int s = host_plan(B, Hq, Hkv, Q_LEN, KV_LEN, d, out_dtype, &P);
+  if (s != FA_OK) return (fa_status)s;
+  if (workspace_bytes < 2 * P.slot_bytes) return FA_ERR_BUFFER_TOO_SMALL;
+  if (reinterpret_cast<uintptr_t>(dev_workspace) & 255u) return FA_ERR_INVALID_ARG;
+  const fa_block_mask& M = *block_mask;
+  if (M.q_len != Q_LEN || M.kv_len != KV_LEN || !(M.Bm == 1 || M.Bm == B) || !(M.Hm == 1 || M.Hm == Hq))
+    return FA_ERR_SHAPE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t s_in = nullptr, s_out = nullptr, s_c1 = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_in[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr},
+              ev_free[2] = {nullptr, nullptr};
+  bool cuda_ok = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaStreamCreateWithFlags(&s_c1, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; i < 2 && cuda_ok; ++i)
+    cuda_ok = cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&ev_done[i], cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&ev_free[i], cudaEventDisableTiming) == cudaSuccess;
+  // the side streams start after everything already queued on `stream` (e.g. the mask build)
+  if (cuda_ok) cuda_ok = cudaEventRecord(ev_start, st) == cudaSuccess && cudaStreamWaitEvent(s_in, ev_start, 0) ==
+                         cudaSuccess && cudaStreamWaitEvent(s_out, ev_start, 0) == cudaSuccess &&
+                         cudaStreamWaitEvent(s_c1, ev_start, 0) == cudaSuccess;
+  const size_t qh = (size_t)Q_LEN * d, kh = (size_t)KV_LEN * d;
+  const size_t oel = out_dtype == FA_OUT_F32 ? 4 : 2;
+  int status = cuda_ok ? FA_OK : FA_ERR_CUDA;
+  for (int c = 0; c < P.n_chunks && status == FA_OK; ++c) {
+    const int slot = c & 1;
+    cudaStream_t sc = slot ? s_c1 : st;  // this slot's kernels
+    const int b = c / P.chunks_per_b, hk0 = (c % P.chunks_per_b) * P.ck;
+    const int nk = std::min(P.ck, Hkv - hk0), h0 = hk0 * P.g, nq = nk * P.g;
+    uint8_t* base = static_cast<uint8_t*>(dev_workspace) + slot * P.slot_bytes;
+    void* dq = base;
+    void* dk = base + P.q_bytes;
+    void* dv = base + P.q_bytes + P.kv_bytes;
+    void* dout = base + P.q_bytes + 2 * P.kv_bytes;
+    float* dlse = reinterpret_cast<float*>(base + P.q_bytes + 2 * P.kv_bytes + P.o_bytes);
+    // copies in, once the copies out of the chunk that used this slot before have finished
+    if (c >= 2 && cudaStreamWaitEvent(s_in, ev_free[slot], 0) != cudaSuccess) { status = FA_ERR_CUDA; break; }
+    const size_t qoff = ((size_t)b * Hq + h0) * qh, koff = ((size_t)b * Hkv + hk0) * kh;
+    if (cudaMemcpyAsync(dq, static_cast<const uint8_t*>(host_q) + qoff * 2, (size_t)nq * qh * 2,
+                        cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+        cudaMemcpyAsync(dk, static_cast<const uint8_t*>(host_k) + koff * 2, (size_t)nk * kh * 2,
+                        cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+        cudaMemcpyAsync(dv, static_cast<const uint8_t*>(host_v) + koff * 2, (size_t)nk * kh * 2,
+                        cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+        cudaEventRecord(ev_in[slot], s_in) != cudaSuccess || cudaStreamWaitEvent(sc, ev_in[slot], 0) != cudaSuccess) {
+      status = FA_ERR_CUDA;
+      break;
+    }
+    // the chunk's view of the mask, the rules and the score: batch row b, heads h0 .. h0 + nq - 1
+    fa_block_mask V = M;
+    size_t row0 = 0;
+    if (M.Bm > 1) row0 += (size_t)b * M.Hm * M.nq;
+    if (M.Hm > 1) row0 += (size_t)h0 * M.nq;
+    V.Bm = 1;
+    V.Hm = M.Hm > 1 ? nq : 1;
+    V.kv_num = M.kv_num + row0;
+    V.full_kv_num = M.full_kv_num + row0;
+    V.kv_idx = M.kv_idx + row0 * M.nk;
+    V.full_kv_idx = M.full_kv_idx + row0 * M.nk;
+    V.q_num = V.q_idx = V.full_q_num = V.full_q_idx = nullptr;  // the forward reads the row tables only
+    V.block_class = M.block_class ? M.block_class + row0 * M.nk : nullptr;
+    if (M.rule.q_offset) V.rule.q_offset = M.rule.q_offset + (M.Bm > 1 ? b : 0);
+    if (M.rule.doc_ids && M.rule.doc_batch > 1) {
+      V.rule.doc_ids = M.rule.doc_ids + (size_t)b * M.rule.doc_len;
+      V.rule.doc_batch = 1;
+      if (M.doc_run) V.doc_run = M.doc_run + (size_t)b * 2 * M.rule.doc_len;
+      if (M.doc_sorted) V.doc_sorted = M.doc_sorted + b;
+    }
+    fa_score_rule S;
+    const fa_score_rule* Sp = nullptr;
+    if (score_rule) {
+      S = *score_rule;
+      if (S.alibi_slopes) S.alibi_slopes += h0;
+      if (S.rel_bias) S.rel_bias += (size_t)h0 * (2 * (size_t)KV_LEN - 1);
+      Sp = &S;
+    }
+    s = forward_impl(false, dq, dk, dv, &V, Sp, scale, dout, out_dtype, dlse, 1, nq, nk, Q_LEN, KV_LEN, d, dev_status,
+                     nullptr, reinterpret_cast<fa_stream_t>(sc));
+    if (s != FA_OK) { status = s; break; }
+    // copies out
+    if (cudaEventRecord(ev_done[slot], sc) != cudaSuccess || cudaStreamWaitEvent(s_out, ev_done[slot], 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<uint8_t*>(host_out) + qoff * oel, dout, (size_t)nq * qh * oel,
+                        cudaMemcpyDeviceToHost, s_out) != cudaSuccess ||
+        cudaMemcpyAsync(host_lse + ((size_t)b * Hq + h0) * Q_LEN, dlse, (size_t)nq * Q_LEN * 4, cudaMemcpyDeviceToHost,
+                        s_out) != cudaSuccess ||
+        cudaEventRecord(ev_free[slot], s_out) != cudaSuccess) {
+      status = FA_ERR_CUDA;
+      break;
+    }
+  }
+  // `stream` completes after the last copy out; the side streams and events are released when idle
+  if (s_out && cudaEventRecord(ev_start, s_out) == cudaSuccess) cudaStreamWaitEvent(st, ev_start, 0);
+  if (s_c1 && ev_in[0] && cudaEventRecord(ev_in[0], s_c1) == cudaSuccess) cudaStreamWaitEvent(st, ev_in[0], 0);
+  for (int i = 0; i < 2; ++i) {
+    if (ev_in[i]) cudaEventDestroy(ev_in[i]);
+    if (ev_done[i]) cudaEventDestroy(ev_done[i]);
+    if (ev_free[i]) cudaEventDestroy(ev_free[i]);
+  }
+  if (ev_start) cudaEventDestroy(ev_start);
+  if (s_in) cudaStreamDestroy(s_in);
+  if (s_out) cudaStreamDestroy(s_out);
+  if (s_c1) cudaStreamDestroy(s_c1);
+  return (fa_status)status;
+}
+
 fa_status fa_flex_forward_mma(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
                               const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype,
                               float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN,

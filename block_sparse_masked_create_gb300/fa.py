@@ -86,6 +86,11 @@ def load() -> ctypes.CDLL:
     lib.fa_block_mask_select_bytes.argtypes = [P(BlockMaskC), i32]
     lib.fa_block_mask_select_rows.restype = ctypes.c_int
     lib.fa_block_mask_select_rows.argtypes = [P(BlockMaskC), vp, i32, vp, sz, P(BlockMaskC), vp, vp]
+    lib.fa_forward_host_workspace_bytes.restype = sz
+    lib.fa_forward_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.fa_flex_forward_host.restype = ctypes.c_int
+    lib.fa_flex_forward_host.argtypes = [vp, vp, vp, P(BlockMaskC), P(ScoreRule), f32, vp, i32, vp, i32, i32, i32, i32,
+                                         i32, i32, vp, sz, vp, vp]
     lib.fa_flex_forward_paged.restype = ctypes.c_int
     lib.fa_flex_forward_paged.argtypes = [vp, vp, vp, vp, i32, i32, i32, P(BlockMaskC), P(ScoreRule), f32, vp, i32, vp,
                                           i32, i32, i32, i32, i32, i32, vp, vp]
@@ -307,6 +312,38 @@ def flex_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: 
     _check(fn(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(block_mask.c), ctypes.byref(score) if score else None,
               float(scale) if scale else 0.0, _ptr(out), _out_code(out), _ptr(lse), B, Hq, Hkv, Q_LEN, KV_LEN, d,
               _ptr(status), _ptr(counters), _stream(q.device)), "fa_flex_forward")
+    return out, lse
+
+
+def forward_host_workspace_bytes(B: int, Hq: int, Hkv: int, Q_LEN: int, KV_LEN: int, d: int,
+                                 out_dtype=torch.bfloat16) -> int:
+    return int(load().fa_forward_host_workspace_bytes(B, Hq, Hkv, Q_LEN, KV_LEN, d,
+                                                      1 if out_dtype == torch.float32 else 0))
+
+
+def flex_forward_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: BlockMask,
+                      score: Optional[ScoreRule] = None, scale: Optional[float] = None,
+                      out: torch.Tensor = None, lse: torch.Tensor = None, workspace: torch.Tensor = None,
+                      status: Optional[torch.Tensor] = None, device=None):
+    """fa_flex_forward_host: q/k/v (bf16), out (bf16 or fp32) and lse (fp32) are host tensors (pin them for
+    full copy speed); the chunks stream through `workspace` on `device`. Returns (out, lse) once the
+    current stream of `device` has been synchronised by the caller."""
+    for t in (q, k, v, out, lse):
+        if t is None or t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, out, lse must be contiguous host tensors")
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("q, k, v must be bf16")
+    B, Hq, Q_LEN, d = q.shape
+    Hkv, KV_LEN = k.shape[1], k.shape[2]
+    dev = torch.device(device) if device is not None else block_mask.buf.device
+    if workspace is None:
+        workspace = torch.empty(forward_host_workspace_bytes(B, Hq, Hkv, Q_LEN, KV_LEN, d, out.dtype),
+                                dtype=torch.uint8, device=dev)
+    _check(load().fa_flex_forward_host(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(block_mask.c),
+                                       ctypes.byref(score) if score else None, float(scale) if scale else 0.0,
+                                       _ptr(out), _out_code(out), _ptr(lse), B, Hq, Hkv, Q_LEN, KV_LEN, d,
+                                       _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev)),
+           "fa_flex_forward_host")
     return out, lse
 
 

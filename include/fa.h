@@ -199,6 +199,25 @@ FA_API fa_status fa_flex_forward(const void* q, const void* k, const void* v, co
                                  float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN,
                                  int32_t d, int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream);
 
+/* The same forward with Q, K, V, O and LSE in host memory (pinned memory for full copy speed), for callers
+ * whose tensors live on the host: the batch's KV heads are cut into chunks (about eight per call) that
+ * stream through two device slots of `dev_workspace`; each chunk's copies in, its kernel and its copies
+ * out run on separate streams, so copies overlap the neighbouring chunks' work. The mask stays on the
+ * device (build it with fa_create_block_mask on `stream` first).
+ *   host_q, host_k, host_v, host_out, host_lse  host pointers, layouts as fa_flex_forward; they must stay
+ *                valid until `stream` has completed
+ *   dev_workspace  device buffer of >= fa_forward_host_workspace_bytes(...) bytes, 256-byte aligned
+ *   stream       everything queued on it before the call runs first; the call's last copy out completes
+ *                on it (synchronise `stream` before reading host_out / host_lse)
+ * Returns the errors of fa_flex_forward, FA_ERR_BUFFER_TOO_SMALL, FA_ERR_CUDA (stream or event creation). */
+FA_API size_t fa_forward_host_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN,
+                                              int32_t d, int32_t out_dtype);
+FA_API fa_status fa_flex_forward_host(const void* host_q, const void* host_k, const void* host_v,
+                                      const fa_block_mask* block_mask, const fa_score_rule* score_rule, float scale,
+                                      void* host_out, int32_t out_dtype, float* host_lse, int32_t B, int32_t Hq,
+                                      int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d, void* dev_workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, fa_stream_t stream);
+
 /* The same forward with K and V in a paged cache ("5.1.2 FlexAttention ...", section 5, the paragraph on
  * turning the logical BlockMask into physical pages; "FlexAttention: compiler optimisation ...", section
  * 6): the rules stay in logical positions (the mask, causal / window bounds, the score rule and the query

@@ -135,3 +135,49 @@ def test_tc5_matches_mma_kernel_cfg2_small():
     d = (a["out"].float() - b["out"].float()).abs().max().item()
     assert d <= 8e-3
     assert (a["lse"] - b["lse"]).abs().max().item() <= 2e-3
+
+
+@pytest.mark.parametrize("kind", ["causal_mha", "gqa_docs_per_batch_alibi", "head_dependent_window_bf16"])
+def test_forward_from_host_buffers(kind):
+    # fa_flex_forward_host streams chunks of KV heads through two device slots: bit-identical to the
+    # device forward, with per-batch document ids and query offsets, per-head tables and per-head ALiBi
+    # slopes taken at each chunk's offsets
+    dev = "cuda"
+    if kind == "causal_mha":
+        w = workloads.cfg2(B=2, H=6, n=640).generate()
+        doc = off = None
+        out_dtype, hdep = torch.float32, False
+    elif kind == "gqa_docs_per_batch_alibi":
+        w = workloads.Prefill("host_gqa", 3, 8, 2, 384, 384, 128, 128, 128, [("causal",), ("doc",), ("and",)],
+                              {"alibi_slopes": [2.0 ** (-(h + 1)) for h in range(8)]}, 1.0 / math.sqrt(128), 77)
+        w.generate()
+        rng = np.random.default_rng(3)
+        doc = np.sort(rng.integers(0, 5, size=(3, 384)), axis=1).astype(np.int32)
+        off = None
+        out_dtype, hdep = torch.float32, False
+    else:
+        w = workloads.Prefill("host_hdep", 1, 4, 4, 500, 500, 64, 128, 128, [("causal",), ("window", 200), ("and",)],
+                              {}, 1.0 / math.sqrt(64), 78)
+        w.generate()
+        doc = off = None
+        out_dtype, hdep = torch.bfloat16, True
+    doc_t = None if doc is None else torch.from_numpy(doc).to(dev)
+    rule = fa.make_mask_rule(w.rule, doc_ids=doc_t, head_dependent=hdep)
+    bm = fa.create_block_mask(rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk, device=dev, keep=[doc_t])
+    al, rb, sc = gc.score_tensors(w.score, dev)
+    q = workloads.bf16_torch(w.q_bits, dev)
+    k = workloads.bf16_torch(w.k_bits, dev)
+    v = workloads.bf16_torch(w.v_bits, dev)
+    o_dev, l_dev = fa.flex_forward(q, k, v, bm, sc, w.scale, out_dtype=out_dtype)
+    hq = workloads.bf16_torch(w.q_bits).pin_memory()
+    hk = workloads.bf16_torch(w.k_bits).pin_memory()
+    hv = workloads.bf16_torch(w.v_bits).pin_memory()
+    ho = torch.empty(q.shape, dtype=out_dtype).pin_memory()
+    hl = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32).pin_memory()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    fa.flex_forward_host(hq, hk, hv, bm, sc, w.scale, out=ho, lse=hl, status=status)
+    torch.cuda.synchronize()
+    assert fa.check_status(status) == fa.OK
+    assert torch.equal(ho.view(torch.int16 if out_dtype == torch.bfloat16 else torch.int32),
+                       o_dev.cpu().view(torch.int16 if out_dtype == torch.bfloat16 else torch.int32))
+    assert torch.equal(hl.view(torch.int32), l_dev.cpu().view(torch.int32))
