@@ -507,8 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const DevMask& M = a.mask;
-  const int r = M.nq - 1 - (int)blockIdx.x;  // long rows first
   const int h = blockIdx.y, b = blockIdx.z;
+  // long rows first: the mask's row order (causal: nq-1 .. 0)
+  const int r = M.row_order
+                    ? __ldg(M.row_order + ((size_t)(M.Bm > 1 ? b : 0) * M.Hm + (M.Hm > 1 ? h : 0)) * M.nq + blockIdx.x)
+                    : M.nq - 1 - (int)blockIdx.x;
   const int hk = h / (a.Hq / a.Hkv);
   const size_t mrow = ((size_t)(M.Bm > 1 ? b : 0) * M.Hm + (M.Hm > 1 ? h : 0)) * M.nq + r;
   const int nf = __ldg(M.full_kv_num + mrow), n = nf + __ldg(M.kv_num + mrow);

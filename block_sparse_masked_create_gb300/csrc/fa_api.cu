@@ -126,6 +126,7 @@ static DevMask dev_mask(const fa_block_mask* m) {
   d.q_idx = m->q_idx;
   d.full_q_num = m->full_q_num;
   d.full_q_idx = m->full_q_idx;
+  d.row_order = m->row_order;
   return d;
 }
 
@@ -136,7 +137,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct MaskLayout {
   int Bm, Hm, nq, nk;
-  size_t off[11];  // the nine tables, then document run bounds and sortedness flags (document rules)
+  size_t off[12];  // the nine tables, document run bounds and sortedness flags (document rules), row order
   size_t total;
 };
 
@@ -160,10 +161,10 @@ static int mask_layout(const fa_mask_rule* rule, int B, int H, int Q_LEN, int KV
   const size_t grid = heads * (size_t)L->nq * L->nk;
   const bool doc = rule_reads_doc(rule) && rule->doc_len > 0 && rule->doc_batch > 0;
   const size_t nb = doc ? (size_t)rule->doc_batch : 0, dl = doc ? (size_t)rule->doc_len : 0;
-  const size_t sizes[11] = {rowsz, rowsz, colsz, colsz, grid * 4, grid * 4, grid * 4, grid * 4, grid,
-                            nb * 2 * dl * sizeof(int32_t), nb * sizeof(int32_t)};
+  const size_t sizes[12] = {rowsz, rowsz, colsz, colsz, grid * 4, grid * 4, grid * 4, grid * 4, grid,
+                            nb * 2 * dl * sizeof(int32_t), nb * sizeof(int32_t), rowsz};
   size_t o = 0;
-  for (int i = 0; i < 11; ++i) {
+  for (int i = 0; i < 12; ++i) {
     L->off[i] = o;
     o += align256(sizes[i]);
   }
@@ -405,6 +406,7 @@ fa_status fa_create_block_mask(const fa_mask_rule* rule, int32_t B, int32_t H, i
   T.block_class = base + L.off[8];
   T.doc_run = R.any_doc ? reinterpret_cast<int32_t*>(base + L.off[9]) : nullptr;
   T.doc_sorted = R.any_doc ? reinterpret_cast<int32_t*>(base + L.off[10]) : nullptr;
+  T.row_order = reinterpret_cast<int32_t*>(base + L.off[11]);
   if (L.Hm > 65535 || L.Bm > 65535 || L.nq > INT_MAX / 2 || L.nk > 65535 * 1024) return FA_ERR_UNSUPPORTED;
   if (launch_mask_build(R, T, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   out->Bm = T.Bm;
@@ -426,6 +428,7 @@ fa_status fa_create_block_mask(const fa_mask_rule* rule, int32_t B, int32_t H, i
   out->block_class = T.block_class;
   out->doc_run = T.doc_run;
   out->doc_sorted = T.doc_sorted;
+  out->row_order = T.row_order;
   out->rule = *rule;
   return FA_OK;
 }
@@ -524,6 +527,7 @@ fa_status fa_block_mask_select_rows(const fa_block_mask* src, const int32_t* dev
   out->block_class = D.block_class;
   out->doc_run = src->doc_run;  // same document ids, same runs
   out->doc_sorted = src->doc_sorted;
+  out->row_order = nullptr;  // one row per request
   out->rule = src->rule;
   out->rule.q_offset = dev_q_pos;  // the one query row of request b sits at global position q_pos[b]
   out->rule.batch_dependent = 1;
@@ -655,6 +659,7 @@ fa_status fa_flex_forward_host(const void* host_q, const void* host_k, const voi
     V.full_kv_idx = M.full_kv_idx + row0 * M.nk;
     V.q_num = V.q_idx = V.full_q_num = V.full_q_idx = nullptr;  // the forward reads the row tables only
     V.block_class = M.block_class ? M.block_class + row0 * M.nk : nullptr;
+    V.row_order = M.row_order ? M.row_order + row0 : nullptr;
     if (M.rule.q_offset) V.rule.q_offset = M.rule.q_offset + (M.Bm > 1 ? b : 0);
     if (M.rule.doc_ids && M.rule.doc_batch > 1) {
       V.rule.doc_ids = M.rule.doc_ids + (size_t)b * M.rule.doc_len;

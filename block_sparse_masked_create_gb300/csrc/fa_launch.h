@@ -20,6 +20,7 @@ struct DevMask {
   const int32_t* q_idx;
   const int32_t* full_q_num;
   const int32_t* full_q_idx;
+  const int32_t* row_order;    // [Bm,Hm,nq] rows by visited length, longest first (NULL: nq-1 .. 0)
 };
 
 struct MaskOut {
@@ -35,6 +36,7 @@ struct MaskOut {
   uint8_t* block_class;
   int32_t* doc_run;     // [doc_batch][2][doc_len] or NULL
   int32_t* doc_sorted;  // [doc_batch] or NULL
+  int32_t* row_order;   // [Bm][Hm][nq] or NULL
 };
 
 cudaError_t launch_mask_build(const DevRule& R, const MaskOut& T, cudaStream_t st);

@@ -106,9 +106,10 @@ __device__ __forceinline__ Tile make_tile(const FwdArgs& a, int b, int h, int r)
 }
 
 // Work item p -> (batch b, head group hp of NT heads, query block r). The (b, hp) units are taken in groups of
-// kGroupPairs; within a group the query blocks go from the last to the first (heaviest first for causal
-// masks) with the group's pairs side by side, so the CTAs resident at any time share the K / V of a few
-// heads in L2 instead of streaming every head's K / V from DRAM once per query block.
+// kGroupPairs; within a group the query blocks follow the mask's row order (longest rows first, so the
+// short ones fill the tail; for causal masks the last block first) with the group's pairs side by side,
+// so the CTAs resident at any time share the K / V of a few heads in L2 instead of streaming every
+// head's K / V from DRAM once per query block.
 template <int NT>
 __device__ __forceinline__ void work_item(const FwdArgs& a, int p, int& b, int& hp, int& r) {
   const int HP = (a.Hq + NT - 1) / NT;
@@ -120,7 +121,10 @@ __device__ __forceinline__ void work_item(const FwdArgs& a, int p, int& b, int& 
   const int pair = g0 + rem % gs;
   hp = pair % HP;
   b = pair / HP;
-  r = nq - 1 - rem / gs;
+  // query blocks by visited length, longest first (the mask's row order; causal: nq-1 .. 0)
+  const DevMask& M = a.mask;
+  r = M.row_order ? __ldg(M.row_order + ((size_t)(M.Bm > 1 ? b : 0) * M.Hm + (M.Hm > 1 ? NT * hp : 0)) * nq + rem / gs)
+                  : nq - 1 - rem / gs;
 }
 
 template <int D, int SK, int NT>

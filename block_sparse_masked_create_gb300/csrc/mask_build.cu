@@ -454,11 +454,70 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
   }
 }
 
+// Rows of the table by visited length (full + partial), longest first, ties by the higher row first:
+// a stable counting sort over the key nk - length, one CTA per (b_m, h_m). The forward and the dQ kernel
+// take their query blocks in this order, so the longest rows start first and the short ones fill the
+// tail ("5.1.2 FlexAttention ...", section 5: row lengths as the load signal). For causal tables this is
+// the order nq-1 .. 0. Tables wider than kOrderBins - 1 blocks keep that order.
+// Runs in one extra CTA per (b_m, h_m) of the transpose launch (the row tables are complete by then).
+constexpr int kOrderBins = 8193;
+
+__device__ void mask_row_order(const MaskOut& T, int hm, int bm, int* s_cnt /* [kOrderBins] */,
+                               int* s_tmp /* [8] */) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int nq = T.nq, nk = T.nk;
+  const size_t base = ((size_t)bm * T.Hm + hm) * nq;
+  int32_t* order = T.row_order + base;
+  if (nk + 1 > kOrderBins) {
+    for (int x = tid; x < nq; x += kThreads) order[x] = nq - 1 - x;
+    return;
+  }
+  auto len = [&](int r) { return __ldg(T.kv_num + base + r) + __ldg(T.full_kv_num + base + r); };
+  for (int x = tid; x <= nk; x += kThreads) s_cnt[x] = 0;
+  __syncthreads();
+  for (int r = tid; r < nq; r += kThreads) atomicAdd(&s_cnt[nk - len(r)], 1);
+  __syncthreads();
+  // exclusive scan of the counts: the first position of each key
+  const int nb = nk + 1, seg = (nb + kThreads - 1) / kThreads;
+  const int s0 = min(tid * seg, nb), s1 = min(s0 + seg, nb);
+  int sum = 0;
+  for (int x = s0; x < s1; ++x) sum += s_cnt[x];
+  const ScanOut so = block_scan2(sum, 0, s_tmp);
+  int run = so.excl_a;
+  for (int x = s0; x < s1; ++x) {
+    const int c = s_cnt[x];
+    s_cnt[x] = run;
+    run += c;
+  }
+  __syncthreads();
+  // placement by one warp, 32 rows per step from the highest row down: lanes with the same key take
+  // consecutive positions in lane order (higher rows first), then the key's cursor moves past them
+  if (tid < 32) {
+    for (int r0 = nq - 1; r0 >= 0; r0 -= 32) {
+      const int r = r0 - lane;
+      const bool valid = r >= 0;
+      const int key = valid ? nk - len(r) : -1 - lane;  // lanes past row 0 get keys of their own
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int pos = valid ? s_cnt[key] + rank : 0;
+      __syncwarp();
+      if (valid && rank == 0) s_cnt[key] += __popc(peers);
+      __syncwarp();
+      if (valid) order[pos] = r;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads) mask_transpose_kernel(DevRule R, MaskOut T) {
   const int c = blockIdx.x, hm = blockIdx.y, bm = blockIdx.z;
   const int tid = threadIdx.x;
   const int nq = T.nq, nk = T.nk;
   __shared__ int s_tmp[8];
+  if (c == nk) {  // the extra CTA: the row order
+    __shared__ int s_cnt[kOrderBins];
+    mask_row_order(T, hm, bm, s_cnt, s_tmp);
+    return;
+  }
   __shared__ Hull s_h;  // the query blocks that can reach this KV block; the class matrix is empty elsewhere
   if (tid == 0) {
     const int64_t off = R.q_offset ? (int64_t)__ldg(R.q_offset + bm) : 0;
@@ -624,7 +683,8 @@ cudaError_t launch_mask_build(const DevRule& R0, const MaskOut& T, cudaStream_t 
   mask_classify_kernel<<<g1, kThreads, 0, st>>>(R, T);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 g2(T.nk, T.Hm, T.Bm);
+
+  dim3 g2(T.nk + (T.row_order ? 1 : 0), T.Hm, T.Bm);  // + one CTA per (b_m, h_m) for the row order
   mask_transpose_kernel<<<g2, kThreads, 0, st>>>(R, T);
   return cudaGetLastError();
 }

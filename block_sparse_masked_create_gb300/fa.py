@@ -49,7 +49,7 @@ class BlockMaskC(ctypes.Structure):
                 ("full_kv_idx", ctypes.c_void_p), ("q_num", ctypes.c_void_p), ("q_idx", ctypes.c_void_p),
                 ("full_q_num", ctypes.c_void_p), ("full_q_idx", ctypes.c_void_p),
                 ("block_class", ctypes.c_void_p), ("doc_run", ctypes.c_void_p), ("doc_sorted", ctypes.c_void_p),
-                ("rule", MaskRule)]
+                ("row_order", ctypes.c_void_p), ("rule", MaskRule)]
 
 
 _lib = None
@@ -223,6 +223,8 @@ class BlockMask:
                              ("full_q_idx", Bm * Hm * nk * nq, (Bm, Hm, nk, nq))):
             out[name] = self._view(getattr(c, name), n, torch.int32).view(shp)
         out["block_class"] = self._view(c.block_class, Bm * Hm * nq * nk, torch.uint8).view(Bm, Hm, nq, nk)
+        if c.row_order:
+            out["row_order"] = self._view(c.row_order, Bm * Hm * nq, torch.int32).view(Bm, Hm, nq)
         return out
 
 

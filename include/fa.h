@@ -127,6 +127,10 @@ typedef struct {
                                and one-past-last position of the run of equal ids around it; else NULL */
   int32_t* doc_sorted;      /* [doc_batch]: 1 where the ids never decrease (each id is then one run, and
                                the kernels test document equality as a column interval); else NULL */
+  int32_t* row_order;       /* [Bm,Hm,nq]: the query block rows by visited length (full + partial) from the
+                               longest, ties by the higher row first ("5.1.2 FlexAttention ...", section 5:
+                               row lengths as the load signal; longest work first). The forward and the
+                               dQ kernel take their query blocks in this order. NULL: rows nq-1 .. 0. */
   fa_mask_rule rule;
 } fa_block_mask;
 

@@ -120,6 +120,19 @@ def tables_np(bm: fa.BlockMask) -> dict:
     return {k: v.cpu().numpy() for k, v in t.items()}
 
 
+def assert_row_order(got: dict, want: dict):
+    """The builder's row order: query block rows by visited length (full + partial) from the longest, ties
+    by the higher row first; derived here from the oracle's tables with a stable sort."""
+    ln = want["kv_num"] + want["full_kv_num"]                        # [Bm, Hm, nq]
+    nq = ln.shape[2]
+    rows_desc = np.arange(nq - 1, -1, -1)
+    for bm in range(ln.shape[0]):
+        for hm in range(ln.shape[1]):
+            l_desc = ln[bm, hm, rows_desc]
+            expect = rows_desc[np.argsort(-l_desc, kind="stable")]
+            assert np.array_equal(got["row_order"][bm, hm], expect), f"row order ({bm},{hm})"
+
+
 def assert_tables_equal(got: dict, want: dict, rows=None):
     keys = ["kv_num", "kv_idx", "full_kv_num", "full_kv_idx", "block_class"]
     for k in keys:

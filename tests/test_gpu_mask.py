@@ -10,7 +10,7 @@ import torch
 
 from block_sparse_masked_create_gb300 import fa, workloads
 from oracle import flexmask_oracle as orc
-from tests.gpu_common import assert_tables_equal, tables_np
+from tests.gpu_common import assert_row_order, assert_tables_equal, tables_np
 
 pytestmark = pytest.mark.gpu
 
@@ -118,6 +118,7 @@ def test_workload_tables(name):
     bm, t = gpu_tables(w.rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk, doc=w.doc_ids)
     want = orc.block_mask(w.rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk, doc_ids=w.doc_ids)
     assert_tables_equal(t, want)
+    assert_row_order(t, want)
     st = fa.block_mask_stats(bm).cpu().tolist()
     cls = want["block_class"]
     assert st[0] == int((cls == 2).sum()) and st[1] == int((cls == 1).sum()) and st[2] == int((cls == 0).sum())
@@ -205,6 +206,7 @@ def test_hull_random_rules(seed):
     want = orc.block_mask(spec, B, 1, q_len, kv_len, bq, bk, batch_dependent=True, q_offset=off,
                           doc_ids=doc if uses_doc else None)
     assert_tables_equal(t, want)
+    assert_row_order(t, want)
 
 
 def test_long_window_table_o_visited():
