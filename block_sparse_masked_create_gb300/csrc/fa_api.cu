@@ -406,7 +406,7 @@ fa_status fa_create_block_mask(const fa_mask_rule* rule, int32_t B, int32_t H, i
   T.block_class = base + L.off[8];
   T.doc_run = R.any_doc ? reinterpret_cast<int32_t*>(base + L.off[9]) : nullptr;
   T.doc_sorted = R.any_doc ? reinterpret_cast<int32_t*>(base + L.off[10]) : nullptr;
-  T.row_order = reinterpret_cast<int32_t*>(base + L.off[11]);
+  T.row_order = L.nq > 1 ? reinterpret_cast<int32_t*>(base + L.off[11]) : nullptr;  // one row: nothing to order
   if (L.Hm > 65535 || L.Bm > 65535 || L.nq > INT_MAX / 2 || L.nk > 65535 * 1024) return FA_ERR_UNSUPPORTED;
   if (launch_mask_build(R, T, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   out->Bm = T.Bm;

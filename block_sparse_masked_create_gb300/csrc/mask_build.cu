@@ -458,9 +458,10 @@ __global__ void __launch_bounds__(kThreads) mask_classify_kernel(DevRule R, Mask
 // a stable counting sort over the key nk - length, one CTA per (b_m, h_m). The forward and the dQ kernel
 // take their query blocks in this order, so the longest rows start first and the short ones fill the
 // tail ("5.1.2 FlexAttention ...", section 5: row lengths as the load signal). For causal tables this is
-// the order nq-1 .. 0. Tables wider than kOrderBins - 1 blocks keep that order.
-// Runs in one extra CTA per (b_m, h_m) of the transpose launch (the row tables are complete by then).
-constexpr int kOrderBins = 8193;
+// the order nq-1 .. 0. Tables wider than kOrderBins - 1 blocks (keys past 2048 x Bk) keep that order.
+// Runs in one extra CTA per (b_m, h_m) of the transpose launch (the row tables are complete by then);
+// the histogram is static shared memory of every CTA of that launch, hence kept small.
+constexpr int kOrderBins = 2049;
 
 __device__ void mask_row_order(const MaskOut& T, int hm, int bm, int* s_cnt /* [kOrderBins] */,
                                int* s_tmp /* [8] */) {

@@ -130,7 +130,8 @@ typedef struct {
   int32_t* row_order;       /* [Bm,Hm,nq]: the query block rows by visited length (full + partial) from the
                                longest, ties by the higher row first ("5.1.2 FlexAttention ...", section 5:
                                row lengths as the load signal; longest work first). The forward and the
-                               dQ kernel take their query blocks in this order. NULL: rows nq-1 .. 0. */
+                               dQ kernel take their query blocks in this order. NULL (one row per table):
+                               rows nq-1 .. 0. Tables of more than 2048 key blocks keep nq-1 .. 0 too. */
   fa_mask_rule rule;
 } fa_block_mask;
 
