@@ -386,7 +386,8 @@ def ours(args, rank, world, local_rank):
                      "frac": achieved / pk["bf16"], "traffic": traffic,
                      "kernel": "fa_flex_forward", "peak_src": f"{pk['src']} bf16 burst"},
         "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": args.steps * 3,
+        # per step: mask classify + transpose (with the row order) [+ document runs] + the forward
+        "gpu_launches": args.steps * (3 + (1 if w.doc_ids is not None else 0)),
         "clocks": clk.summary(), "status": fa.status_string(st_code), "wall_s": wall,
     }
     if dec_line:
