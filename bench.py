@@ -5,7 +5,9 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--w
 
 A step = fa_create_block_mask + fa_flex_forward over the whole workload (default: plain causal, B=4,
 Hq=Hkv=16, N=4096, d=128, 128x128 blocks). value = physical TFLOP/s (4*d*Bq*Bk per visited block per
-(b,h)) of the whole step, all ranks. One JSON line on rank 0.
+(b,h)) of the whole step, all ranks. The other prefill workloads (document-causal + ALiBi N=16384; sliding
+window 1024 + soft-cap N=65536) are timed the same way and reported as objects of the same line, beside
+the paged decode, the backward and the paged prefill. One JSON line on rank 0.
 """
 from __future__ import annotations
 
@@ -39,6 +41,7 @@ def parse():
     p.add_argument("--decode-requests", type=int, default=64, help="requests in the decode batch")
     p.add_argument("--no-backward", action="store_true")
     p.add_argument("--no-paged", action="store_true")
+    p.add_argument("--no-others", action="store_true", help="skip the other prefill workloads")
     p.add_argument("--backward-only", action="store_true",
                    help="after the forward, time only the backward and print its object as the line (profiling aid)")
     return p.parse_args()
@@ -57,11 +60,6 @@ def peaks():
 def make_workload(name):
     from block_sparse_masked_create_gb300 import workloads
     return {"cfg2": workloads.cfg2, "cfg3": workloads.cfg3, "cfg4": workloads.cfg4}[name]()
-
-
-def visited_blocks(w):
-    """Visited (full + partial) blocks per mask row, from the oracle-free block counts of the device table."""
-    return None
 
 
 class ClockSampler:
@@ -136,11 +134,12 @@ sys.path.insert(0, %(root)r)
 from block_sparse_masked_create_gb300 import workloads, synth
 from oracle import flexmask_oracle as orc
 w = workloads.%(wl)s()
-rng = np.random.default_rng(0)
+rng = np.random.default_rng(%(seed)d)
 g = w.Hq // w.Hkv
 n_q = -(-w.q_len // w.bq)
+score = {k: (np.asarray(v, np.float64) if k != 'softcap' else v) for k, v in w.score.items()}
 times, flops = [], []
-for it in range(%(reps)d):
+while len(times) < %(reps)d and sum(times) < %(seconds)f:
     b, h, r = int(rng.integers(w.B)), int(rng.integers(w.Hq)), int(rng.integers(n_q))
     rows = np.arange(r * w.bq, min(w.q_len, (r + 1) * w.bq))
     hk = h // g
@@ -152,13 +151,38 @@ for it in range(%(reps)d):
     t = orc.block_mask(w.rule, 1, 1, w.q_len, w.kv_len, w.bq, w.bk, doc_ids=w.doc_ids, rows=[r])
     vis = int(t["kv_num"][0, 0, r] + t["full_kv_num"][0, 0, r])
     t0 = time.perf_counter()
-    orc.attention_rows(qf, kf, vf, w.rule, rows, b, h, w.q_len, w.kv_len, w.scale,
-                       {k: (np.asarray(v, np.float64) if k != 'softcap' else v) for k, v in w.score.items()},
-                       0, w.doc_ids)
+    orc.attention_rows(qf, kf, vf, w.rule, rows, b, h, w.q_len, w.kv_len, w.scale, score, 0, w.doc_ids)
     times.append(time.perf_counter() - t0)
     flops.append(4.0 * w.d * w.bq * w.bk * vis)
 print(json.dumps({"times": times, "flops": flops}))
 """
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_oracle_parallel(wl: str, reps: int, seconds: float, workers: int) -> dict:
+    """The oracle as it stands on `workers` host cores: one single-threaded worker process per core, each
+    timing the oracle on its own seeded sample of query-block rows (at most `reps` rows or `seconds` of
+    oracle time). The processes are started with exec (no fork of a CUDA context)."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    procs = [subprocess.Popen([sys.executable, "-c", CPU_SNIPPET % dict(root=ROOT, wl=wl, reps=reps,
+                                                                        seconds=seconds, seed=i)],
+                              stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env)
+             for i in range(workers)]
+    res = []
+    for p in procs:
+        out, err = p.communicate(timeout=1800)
+        if p.returncode != 0:
+            raise RuntimeError(err[-2000:])
+        res.append(json.loads(out.strip().splitlines()[-1]))
+    return {"workers": res}
 
 
 def max_over_ranks(ms: float, dist=None, device=None) -> float:
@@ -176,34 +200,25 @@ def job_tflops(world: int, flop_per_rank: float, ms_step: float) -> float:
     return world * flop_per_rank / (ms_step * 1e-3) / 1e12
 
 
-def run_oracle_sample(wl: str, reps: int) -> dict:
-    env = dict(os.environ)
-    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
-        env[k] = "1"
-    code = CPU_SNIPPET % dict(root=ROOT, wl=wl, reps=reps)
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
-    if r.returncode != 0:
-        raise RuntimeError(r.stderr[-2000:])
-    return json.loads(r.stdout.strip().splitlines()[-1])
-
-
 def reference_arm(args, rank):
     if rank != 0:
         return
     w = make_workload(args.workload)
-    reps = args.warmup + args.steps
-    res = run_oracle_sample(args.workload, reps)
-    t = res["times"][args.warmup:]
-    f = res["flops"][args.warmup:]
-    value = sum(f) / sum(t) / 1e12
+    cores = host_cores()
+    # a step = one query-block row of a random (b, h) on every host core, in parallel
+    res = run_oracle_parallel(args.workload, args.warmup + args.steps, 1e9, cores)["workers"]
+    t_w = [sum(r["times"][args.warmup:]) for r in res]
+    f_tot = sum(sum(r["flops"][args.warmup:]) for r in res)
+    value = f_tot / max(t_w) / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(t) / len(t), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * max(t_w) / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} N={w.q_len} d={w.d} Bq=Bk={w.bq}",
-                   "step": "oracle on one query block row (Bq rows) of a random (b, h)"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} timed query-block rows of {w.bq} queries (fp64 numpy, 1 thread)"},
+                   "step": f"oracle on one query block row (Bq rows) of a random (b, h) per host core, {cores} cores"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} timed query-block rows of {w.bq} queries per core "
+                                   f"(fp64 numpy, one single-threaded process per core)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -212,11 +227,197 @@ def reference_arm(args, rank):
 # ------------------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------------------
-def ours(args, rank, world, local_rank):
-    import numpy as np
+LOGICAL_NOTE = "valid (query, key) pairs from the rule's closed form"
+
+
+def logical_pairs_of(name, w):
+    """Exact count of allowed (query, key) pairs of a prefill workload, from closed forms of its rule
+    (causal: n(n+1)/2 per head; window W: W(W+1)/2 + (n-W)W; document-causal: sum of len(len+1)/2)."""
+    if name == "cfg2":
+        return w.B * w.Hq * w.q_len * (w.q_len + 1) // 2
+    if name == "cfg4":
+        W = 1024
+        return w.B * w.Hq * (W * (W + 1) // 2 + (w.q_len - W) * W)
+    if name == "cfg3":
+        return w.B * w.Hq * int(sum(int(L) * (int(L) + 1) // 2 for L in w.doc_lens))
+    return None
+
+
+class Prefill:
+    """One prefill workload resident on the device: inputs, rule, BlockMask, outputs (fp32 O, as the
+    tolerance needs), and the work counts of its visited blocks."""
+
+    def __init__(self, name, dev):
+        import numpy as np
+        import torch
+
+        from block_sparse_masked_create_gb300 import fa, workloads
+        self.name = name
+        w = self.w = make_workload(name).generate()
+        self.q = workloads.bf16_torch(w.q_bits, dev)
+        self.k = workloads.bf16_torch(w.k_bits, dev)
+        self.v = workloads.bf16_torch(w.v_bits, dev)
+        self.doc = None if w.doc_ids is None else torch.from_numpy(w.doc_ids.astype(np.int32)).to(dev)
+        al = None
+        if w.score.get("alibi_slopes") is not None:
+            al = torch.tensor(np.asarray(w.score["alibi_slopes"], np.float32), device=dev)
+        self.al = al
+        self.sc = fa.make_score_rule(al, None, w.score.get("softcap", 0.0))
+        self.rule = fa.make_mask_rule(w.rule, doc_ids=self.doc)
+        self.bm = fa.create_block_mask(self.rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk, device=dev,
+                                       keep=[self.doc])
+        self.out = torch.empty(self.q.shape, dtype=torch.float32, device=dev)
+        self.lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stats = fa.block_mask_stats(self.bm).cpu().tolist()
+        heads = w.B * w.Hq // (self.bm.c.Bm * self.bm.c.Hm)
+        self.visited = (self.stats[0] + self.stats[1]) * heads
+        self.phys_flops = 4.0 * w.d * w.bq * w.bk * self.visited
+        self.logical_pairs = logical_pairs_of(name, w)
+        self.launches = 3 + (1 if w.doc_ids is not None else 0)   # doc runs, classify, transpose, forward
+
+    def mask(self):
+        from block_sparse_masked_create_gb300 import fa
+        w = self.w
+        fa.recreate_block_mask(self.bm, self.rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk)
+
+    def forward(self):
+        from block_sparse_masked_create_gb300 import fa
+        fa.flex_forward(self.q, self.k, self.v, self.bm, self.sc, self.w.scale, out=self.out, lse=self.lse,
+                        status=self.status)
+
+    def step(self):
+        self.mask()
+        self.forward()
+
+    def row_lengths(self):
+        """Visited blocks (full + partial) per query block row of the table: mean, P50, P95, max ([FX] 5:
+        row lengths as the load signal)."""
+        import numpy as np
+        t = self.bm.tables()
+        ln = (t["kv_num"] + t["full_kv_num"]).flatten().cpu().numpy().astype(np.float64)
+        return {"mean": float(ln.mean()), "p50": float(np.percentile(ln, 50)), "p95": float(np.percentile(ln, 95)),
+                "max": int(ln.max()), "rows": int(ln.size), "nk": int(self.bm.c.nk)}
+
+    def config(self):
+        w = self.w
+        return f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} N={w.q_len} d={w.d} Bq=Bk={w.bq}"
+
+
+def timed_steps(pf, steps, stream):
+    """Per step: events around the mask build and the forward on the launching stream."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        pf.mask()
+        ev[i][1].record(stream)
+        pf.forward()
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return (start.elapsed_time(end), [a.elapsed_time(c) for (_, a, c) in ev],
+            [s_.elapsed_time(a) for (s_, a, _) in ev])
+
+
+def prefill_summary(pf, pk, fwd_ms, mask_ms, ms_step, world):
+    """The per-workload fields: physical and logical TFLOP/s, the forward's roofline, rho_tile, blocks and
+    row lengths."""
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    achieved = pf.phys_flops / (fwd_avg * 1e-3) / 1e12
+    logical = pf.logical_pairs
+    return {
+        "workload": pf.config(),
+        "physical_tflop_per_step": pf.phys_flops / 1e12,
+        "step_tflops": world * pf.phys_flops / (ms_step * 1e-3) / 1e12,
+        "logical_tflops": (world * 4.0 * pf.w.d * logical / (ms_step * 1e-3) / 1e12) if logical else None,
+        "logical_pairs_note": LOGICAL_NOTE,
+        "rho_tile": (pf.phys_flops / (4.0 * pf.w.d * logical)) if logical else None,
+        "pct_bf16_peak": achieved / pk["bf16"],
+        "mask_build_us": 1e3 * statistics.median(mask_ms),
+        "forward_ms_median": statistics.median(fwd_ms),
+        "forward_ms_mean": fwd_avg,
+        "blocks": {"full": pf.stats[0], "partial": pf.stats[1], "empty": pf.stats[2], "row_max": pf.stats[3],
+                   "visited_total": pf.visited},
+        "row_length": pf.row_lengths(),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": achieved / pk["bf16"], "traffic": load_traffic(pf.name),
+                     "kernel": "fa_flex_forward", "peak_src": f"{pk['src']} bf16 burst"},
+    }
+
+
+def other_prefill(name, args, dev, pk, world):
+    """Another prefill workload timed the same way as the main one (mask build + forward per step)."""
     import torch
 
-    from block_sparse_masked_create_gb300 import fa, workloads
+    from block_sparse_masked_create_gb300 import fa
+    pf = Prefill(name, dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        pf.step()
+    torch.cuda.synchronize()
+    ms, fwd_ms, mask_ms = timed_steps(pf, args.steps, stream)
+    o = prefill_summary(pf, pk, fwd_ms, mask_ms, ms / args.steps, world)
+    o["ms_per_step"] = ms / args.steps
+    o["status"] = fa.status_string(fa.check_status(pf.status))
+    o["gpu_launches"] = args.steps * pf.launches
+    return o
+
+
+def copy_ceiling(hq, hk, hv, ho, hl, q, k, v, out, lse, dev):
+    """Plain pinned copies of the e2e step's bytes on their own: all inputs host -> device, all outputs
+    device -> host, and both directions at once on two streams (the floor for any overlap of the two)."""
+    import torch
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    main = torch.cuda.current_stream(dev)
+
+    def h2d():
+        with torch.cuda.stream(s_in):
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s_out):
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+    def timed(fns, n=5):
+        ms = []
+        for it in range(n + 2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(main)
+            for st in (s_in, s_out):
+                st.wait_event(a)
+            for f in fns:
+                f()
+            for st in (s_in, s_out):
+                e = torch.cuda.Event()
+                e.record(st)
+                main.wait_event(e)
+            b.record(main)
+            torch.cuda.synchronize()
+            if it >= 2:
+                ms.append(a.elapsed_time(b))
+        return statistics.median(ms)
+
+    bi = (q.numel() + k.numel() + v.numel()) * 2
+    bo = out.numel() * out.element_size() + lse.numel() * 4
+    t_in, t_out, t_both = timed([h2d]), timed([d2h]), timed([h2d, d2h])
+    return {"h2d_ms": t_in, "d2h_ms": t_out, "duplex_ms": t_both, "h2d_GBps": bi / (t_in * 1e-3) / 1e9,
+            "d2h_GBps": bo / (t_out * 1e-3) / 1e9,
+            "note": "pinned host <-> device copies of the step's input and output bytes alone (CUDA events)"}
+
+
+def ours(args, rank, world, local_rank):
+    import torch
+
+    from block_sparse_masked_create_gb300 import fa
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -225,53 +426,23 @@ def ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     pk = peaks()
-    w = make_workload(args.workload).generate()
-    q = workloads.bf16_torch(w.q_bits, dev)
-    k = workloads.bf16_torch(w.k_bits, dev)
-    v = workloads.bf16_torch(w.v_bits, dev)
-    doc = None if w.doc_ids is None else torch.from_numpy(w.doc_ids.astype(np.int32)).to(dev)
-    al = None
-    if w.score.get("alibi_slopes") is not None:
-        al = torch.tensor(np.asarray(w.score["alibi_slopes"], np.float32), device=dev)
-    sc = fa.make_score_rule(al, None, w.score.get("softcap", 0.0))
-    rule = fa.make_mask_rule(w.rule, doc_ids=doc)
-    bm = fa.create_block_mask(rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk, device=dev, keep=[doc])
-    out = torch.empty(q.shape, dtype=torch.float32, device=dev)   # O stored in fp32 (accumulator precision)
-    lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    stats = fa.block_mask_stats(bm).cpu().tolist()
-    heads = w.B * w.Hq // (bm.c.Bm * bm.c.Hm)
-    visited = (stats[0] + stats[1]) * heads
-    phys_flops = 4.0 * w.d * w.bq * w.bk * visited
-    # logical pairs: exact count from the rule (oracle-free; closed forms of the configs' rules)
-    logical_pairs = None
-    if args.workload == "cfg2":
-        logical_pairs = w.B * w.Hq * w.q_len * (w.q_len + 1) // 2
-    elif args.workload == "cfg4":
-        W = 1024
-        logical_pairs = w.B * w.Hq * (W * (W + 1) // 2 + (w.q_len - W) * W)
-    elif args.workload == "cfg3":
-        logical_pairs = w.B * w.Hq * int(sum(int(L) * (int(L) + 1) // 2 for L in w.doc_lens))
+    pf = Prefill(args.workload, dev)
+    w, q, k, v, out, lse, status, bm, sc = pf.w, pf.q, pf.k, pf.v, pf.out, pf.lse, pf.status, pf.bm, pf.sc
+    phys_flops = pf.phys_flops
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        fa.recreate_block_mask(bm, rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk)
-        fa.flex_forward(q, k, v, bm, sc, w.scale, out=out, lse=lse, status=status)
-
     for _ in range(args.warmup):
-        step()
+        pf.step()
     torch.cuda.synchronize()
     if fa.check_status(status) != fa.OK:
         raise RuntimeError("device status after warm-up")
-    # per-kernel time of the dominant kernel (the forward) with events on the launching stream
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+
     def busy():
         for _ in range(20):
-            step()
+            pf.step()
         torch.cuda.synchronize()
 
     with ClockSampler(local_rank) as clk:
@@ -279,31 +450,18 @@ def ours(args, rank, world, local_rank):
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
-        n_before = len(clk.samples)
         t0 = time.perf_counter()
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            fa.recreate_block_mask(bm, rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk)
-            ev[i][1].record(stream)
-            fa.flex_forward(q, k, v, bm, sc, w.scale, out=out, lse=lse, status=status)
-            ev[i][2].record(stream)
-        end.record(stream)
-        torch.cuda.synchronize()
+        # per-kernel time of the dominant kernel (the forward) with events on the launching stream
+        ms, fwd_ms, mask_ms = timed_steps(pf, args.steps, stream)
         wall = time.perf_counter() - t0
         clk.busy_for(busy, 0.5)
     if dist:
         dist.barrier()
-    ms = max_over_ranks(start.elapsed_time(end), dist, dev)
-    fwd_ms = [a.elapsed_time(c) for (_, a, c) in ev]
-    mask_ms = [s.elapsed_time(a) for (s, a, _) in ev]
+    ms = max_over_ranks(ms, dist, dev)
     st_code = fa.check_status(status)
     ms_step = ms / args.steps
     value = job_tflops(world, phys_flops, ms_step)
-    fwd_avg = sum(fwd_ms) / len(fwd_ms)
-    achieved = phys_flops / (fwd_avg * 1e-3) / 1e12
+    summ = prefill_summary(pf, pk, fwd_ms, mask_ms, ms_step, world)
 
     # ---------------- end to end through the public API with host buffers
     e2e = None
@@ -318,7 +476,7 @@ def ours(args, rank, world, local_rank):
                           dtype=torch.uint8, device=dev)
 
         def e2e_step():  # host tensors in and out: fa_flex_forward_host streams them through the GPU
-            fa.recreate_block_mask(bm, rule, w.B, w.Hq, w.q_len, w.kv_len, w.bq, w.bk)
+            pf.mask()
             fa.flex_forward_host(hq, hk, hv, bm, sc, w.scale, out=ho, lse=hl, workspace=hws, status=status)
 
         for _ in range(max(3, args.warmup // 2)):
@@ -334,8 +492,12 @@ def ours(args, rank, world, local_rank):
         e2e_ms = s2.elapsed_time(e2) / n2
         bi = 3 * q.numel() * 2
         bo = out.numel() * out.element_size() + lse.numel() * 4
+        ceil = copy_ceiling(hq, hk, hv, ho, hl, q, k, v, out, lse, dev)
         e2e = {"value": world * phys_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
+               "api": "fa_flex_forward_host (pinned host Q, K, V, O, LSE)",
+               "copy_ceiling": ceil, "copy_floor_over_e2e": ceil["duplex_ms"] / e2e_ms}
+        del hq, hk, hv, ho, hl, hws
 
     # ---------------- backward over the same mask and forward outputs (secondary line item)
     bwd_line = None
@@ -351,6 +513,16 @@ def ours(args, rank, world, local_rank):
     if not args.no_paged:
         paged_line = bench_paged_prefill(args, dev, pk, w, q, bm, sc, phys_flops)
 
+    # ---------------- the other prefill workloads, each timed like the main one
+    others = {}
+    if not args.no_others:
+        del pf, q, k, v, out, lse
+        torch.cuda.empty_cache()
+        for name in ("cfg2", "cfg3", "cfg4"):
+            if name != args.workload:
+                others[name] = other_prefill(name, args, dev, pk, world)
+                torch.cuda.empty_cache()
+
     # ---------------- decode (secondary metric of the same hot path): paged split-KV, 64 requests
     dec_line = None
     if not args.no_decode:
@@ -358,38 +530,36 @@ def ours(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and not args.no_cpu:
+        cores = host_cores()
+        budget = 20.0
         try:
-            res = run_oracle_sample(args.workload, 6)
-            cpu = {"value": sum(res["flops"]) / sum(res["times"]) / 1e12, "unit": "TFLOP/s", "cores": 1,
-                   "kind": "oracle",
-                   "sample": f"6 query-block rows ({w.bq} queries each) of random (b,h), fp64 numpy, 1 thread; "
-                             f"{sum(res['times']):.1f} s"}
+            res = run_oracle_parallel(args.workload, 10 ** 6, max(1.0, budget / cores), cores)["workers"]
+            t_w = [sum(r["times"]) for r in res]
+            n_rows = sum(len(r["times"]) for r in res)
+            cpu = {"value": sum(sum(r["flops"]) for r in res) / max(t_w) / 1e12, "unit": "TFLOP/s",
+                   "cores": cores, "kind": "oracle",
+                   "sample": f"{n_rows} query-block rows ({w.bq} queries each) of random (b, h) of {w.name}, "
+                             f"fp64 numpy, {cores} single-threaded processes, {sum(t_w):.1f} s of oracle time "
+                             f"({max(t_w):.1f} s wall per core)"}
         except Exception as e:  # reported, never silently replaced
-            cpu = {"value": None, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+            cpu = {"value": None, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": f"failed: {e}"}
 
-    traffic = load_traffic(args.workload)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} N={w.q_len} d={w.d} Bq=Bk={w.bq}",
-                   "step": "fa_create_block_mask + fa_flex_forward", "out": "fp32 O, fp32 LSE",
-                   "l2": "inputs 3x64 MiB + 128 MiB output > 129 MB L2 (no flush)", "parallelism": f"replica x{world} (independent (b,h) shards, no collective)"},
-        "physical_tflop_per_step": phys_flops / 1e12,
-        "logical_tflops": (world * 4.0 * w.d * logical_pairs / (ms_step * 1e-3) / 1e12) if logical_pairs else None,
-        "pct_bf16_peak": value / world / pk["bf16"],
-        "mask_build_us": 1e3 * statistics.median(mask_ms),
-        "forward_ms_median": statistics.median(fwd_ms),
-        "blocks": {"full": stats[0], "partial": stats[1], "empty": stats[2], "row_max": stats[3],
-                   "visited_total": visited},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
-                     "frac": achieved / pk["bf16"], "traffic": traffic,
-                     "kernel": "fa_flex_forward", "peak_src": f"{pk['src']} bf16 burst"},
+        "config": {"workload": pf_config(w), "step": "fa_create_block_mask + fa_flex_forward", "out": "fp32 O, fp32 LSE",
+                   "l2": "inputs larger than the 129 MB L2 (no flush)",
+                   "parallelism": f"replica x{world} (independent (b,h) shards, no collective)"},
+    }
+    line.update({k_: v_ for k_, v_ in summ.items() if k_ != "workload"})
+    line.update({
         "cpu_baseline": cpu, "e2e": e2e,
-        # per step: mask classify + transpose (with the row order) [+ document runs] + the forward
         "gpu_launches": args.steps * (3 + (1 if w.doc_ids is not None else 0)),
         "clocks": clk.summary(), "status": fa.status_string(st_code), "wall_s": wall,
-    }
+    })
+    if others:
+        line["prefill_workloads"] = others
     if dec_line:
         line["decode"] = dec_line
     if bwd_line:
@@ -400,6 +570,10 @@ def ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def pf_config(w):
+    return f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} N={w.q_len} d={w.d} Bq=Bk={w.bq}"
 
 
 def bench_backward(args, dev, pk, w, q, k, v, bm, sc, out, lse, phys_flops):

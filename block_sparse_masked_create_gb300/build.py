@@ -71,7 +71,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in _sources()]
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcuda"] * 0
+        cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

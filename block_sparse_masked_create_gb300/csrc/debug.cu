@@ -144,20 +144,6 @@ __global__ void debug_softcap_kernel(const float* x, float* y, int n, float c) {
   if (i < n) y[i] = softcap_apply(x[i], c, 1.0f / c);
 }
 
-__global__ void debug_exp2_kernel(const float* x, float* y_poly, float* y_mufu, int n) {
-  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
-  if (i >= n) return;
-  const float a = x[i], b = i + 1 < n ? x[i + 1] : 0.f;
-  float p0, p1;
-  f2_unpack(f2_exp2_poly(f2_pack(a, b)), p0, p1);
-  y_poly[i] = p0;
-  y_mufu[i] = ex2_approx(a);
-  if (i + 1 < n) {
-    y_poly[i + 1] = p1;
-    y_mufu[i + 1] = ex2_approx(b);
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_debug_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t st) {
@@ -170,14 +156,6 @@ cudaError_t launch_debug_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t
 extern "C" fa_status fa_debug_softcap(const float* x, float* y, int32_t n, float c, fa_stream_t stream) {
   if (!x || !y || n < 1 || !(c > 0.f)) return FA_ERR_INVALID_ARG;
   fa::debug_softcap_kernel<<<(n + 255) / 256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(x, y, n, c);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
-}
-
-extern "C" fa_status fa_debug_exp2(const float* x, float* y_poly, float* y_mufu, int32_t n, fa_stream_t stream) {
-  if (!x || !y_poly || !y_mufu || n < 1) return FA_ERR_INVALID_ARG;
-  const int pairs = (n + 1) / 2;
-  fa::debug_exp2_kernel<<<(pairs + 127) / 128, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(x, y_poly, y_mufu,
-                                                                                                  n);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -8,6 +8,9 @@
 //
 // Set-up: the first call on a device (with that device current) looks up the array's device address with
 // cudaGetSymbolAddress and caches it for that device. Make that first call before any stream capture.
+// The cached address belongs to the device's context of that moment: after cudaDeviceReset (or anything
+// else that tears down and recreates the context) the module is loaded again and the array may move, which
+// the library cannot see, so this entry point must not be used on that device after such a reset.
 // The array is shared by every call: two calls that overlap on the GPU (different streams, no ordering
 // between them) race on it. Its previous contents never matter: the split kernel writes every slot the
 // combine kernel reads within the same call, so nothing has to be cleared.
@@ -49,9 +52,9 @@ extern "C" fa_status fa_flex_decode_noalloc(const void* q, const void* k_pages, 
                                             float scale, void* out, int32_t out_dtype, float* lse, int32_t Bz,
                                             int32_t Hq, int32_t Hkv, int32_t d, int32_t page, int32_t max_pages,
                                             int32_t* dev_status, int64_t* dev_counters, fa_stream_t stream) {
-  const size_t need = fa_decode_workspace_bytes(Bz, Hq, d, max_pages, page);
-  if (need == 0) return FA_ERR_SHAPE;
-  if (need > fa::kNoAllocScratchBytes) return FA_ERR_BUFFER_TOO_SMALL;  // beyond the fixed scratch size
+  // fa_flex_decode checks every argument first and the workspace size last, so an oversized problem with
+  // otherwise valid arguments returns FA_ERR_BUFFER_TOO_SMALL, and other argument errors keep the codes
+  // they have there; in both cases nothing is launched.
   void* ws = nullptr;
   const int s = fa::scratch_address(&ws);
   if (s != FA_OK) return (fa_status)s;

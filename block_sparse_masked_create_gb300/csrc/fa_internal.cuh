@@ -474,32 +474,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// 2^x for a packed pair on the FMA pipe (relieves the MUFU unit, whose ex2 rate is 4 per clock per SM
-// sub-partition). Range reduction x = k + f with k = round(x) obtained by adding 1.5 * 2^23 (after which the
-// low mantissa bits hold k), f in [-1/2, 1/2]; 2^f by a cubic whose coefficients were fitted for minimax
-// relative error on [-1/2, 1/2] by iteratively reweighted least squares (Lawson's method), max relative
-// error 7.5e-5; 2^k applied by adding k to the exponent field (one integer multiply-add: the constant's
-// own bits vanish in the shift). Inputs are clamped at -126 so the exponent never wraps; -inf gives 0.
-__device__ __forceinline__ uint64_t f2_exp2_poly(uint64_t x2) {
-  float a, b;
-  f2_unpack(x2, a, b);
-  const bool za = a == -INFINITY, zb = b == -INFINITY;
-  const uint64_t xx = f2_pack(fmaxf(a, -126.f), fmaxf(b, -126.f));
-  const uint64_t t = f2_add(xx, f2_pack(12582912.f, 12582912.f));
-  const uint64_t k = f2_add(t, f2_pack(-12582912.f, -12582912.f));
-  const uint64_t f = f2_fma(k, f2_pack(-1.f, -1.f), xx);
-  uint64_t p = f2_fma(f2_pack(0.05517052486538887f, 0.05517052486538887f), f,
-                      f2_pack(0.24260830879211426f, 0.24260830879211426f));
-  p = f2_fma(p, f, f2_pack(0.693260908126831f, 0.693260908126831f));
-  p = f2_fma(p, f, f2_pack(0.9999282360076904f, 0.9999282360076904f));
-  float p0, p1, t0, t1;
-  f2_unpack(p, p0, p1);
-  f2_unpack(t, t0, t1);
-  const float r0 = __uint_as_float(__float_as_uint(t0) * (1u << 23) + __float_as_uint(p0));
-  const float r1 = __uint_as_float(__float_as_uint(t1) * (1u << 23) + __float_as_uint(p1));
-  return f2_pack(za ? 0.f : r0, zb ? 0.f : r1);
-}
-
 // sum of the two bf16 halves of a packed pair, in fp32 (exact widening)
 __device__ __forceinline__ float bf16x2_sum(uint32_t v) {
   return __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);

@@ -7,24 +7,26 @@
 // score rule, -inf for masked pairs (partial blocks only), online softmax (m, l), acc += P V; finally
 // O = acc / l and LSE = m + ln l, an empty row giving O = 0, LSE = -inf.
 //
-// How (one CTA = two 128-row query tiles of sibling heads of the same query block, 10 warps):
-//   warps 0-3 / 4-7  softmax warpgroups of tile 0 / tile 1 (TMEM lane = query row = thread). Per block:
-//                    S from TMEM to registers, score rule, mask, row max (3-input max tree),
-//                    P = 2^(x - m) with packed fp32x2 FMAs, two row sums, P as bf16 back into tensor
-//                    memory over the S columns it came from, "P ready". The O accumulator is rescaled in
-//                    TMEM only when the running max grows by more than 2^8 (exact for any reference max;
-//                    the bound keeps P <= 256). Epilogue O / l -> shared memory -> TMA store.
-//   warp 8           TMA producer: Q tiles, then K / V tiles of the visited blocks only (an empty block
-//                    issues no load) into a 5-slot ring, in exactly the order the MMA warp consumes them.
-//                    Sibling query heads of one KV head with the same mask row share each K / V load.
-//   warp 9           allocates TMEM (S/P and O of both tiles: 512 columns) and issues every tcgen05.mma
-//                    from one thread: when P_t(j) is ready, O_t += P_t(j) V(j) (A read from TMEM) and then
-//                    S_t(j+1) = Q_t K(j+1)^T (A, B from shared memory). The tensor pipe runs a thread's MMAs
-//                    in issue order, so S_t(j+1) overwrites P_t(j) only after the product has read it, and
-//                    the completion of S_t(j) implies that of O_t's previous update.
-// Two tiles in flight keep the tensor core busy while each warpgroup runs its softmax. Every wait is
-// bounded (an abort flag stops all roles; copies and MMAs in flight are drained before tensor memory is
-// freed and the CTA exits).
+// How (one CTA = NT query tiles of 128 rows: two tiles of sibling heads of the same query block in 18
+// warps, or, for short sliding windows of MHA, one tile in 10 warps with two CTAs per SM):
+//   warps 8t .. 8t+7  the softmax of tile t, two warpgroups each owning 64 of a block's 128 key columns
+//                    (TMEM lane = query row = 32 * (warp % 4) + lane). Per block: S from TMEM to
+//                    registers, score rule, mask (partial blocks only), half-row max exchanged through
+//                    shared memory, P = 2^(x - m) with packed fp32x2 FMAs, two row sums, P as bf16 back into
+//                    tensor memory over the S columns it came from, "P ready". The O accumulator is
+//                    rescaled in TMEM only when the running max grows by more than 2^8 (exact for any
+//                    reference max; the bound keeps P <= 256). Epilogue O / l -> shared memory -> TMA store.
+//   warp 8 NT        TMA producer: Q tiles, then K / V tiles of the visited blocks only (an empty block
+//                    issues no load) into a shared-memory ring, in exactly the order the MMA warp consumes
+//                    them. Sibling query heads of one KV head with the same mask row share each K / V load.
+//   warp 8 NT + 1    allocates TMEM (S/P and O of every tile: 256 columns per tile) and issues every
+//                    tcgen05.mma from one thread: when P_t(j) is ready, O_t += P_t(j) V(j) (A read from
+//                    TMEM) and then S_t(j+1) = Q_t K(j+1)^T (A, B from shared memory). The tensor pipe runs a
+//                    thread's MMAs in issue order, so S_t(j+1) overwrites P_t(j) only after the product has
+//                    read it, and the completion of S_t(j) implies that of O_t's previous update.
+// Two tiles in flight keep the tensor core busy while each tile's softmax runs. Every wait is bounded (an
+// abort flag stops all roles; copies and MMAs in flight are drained before tensor memory is freed and the
+// CTA exits).
 #include <cstring>
 
 #include "fa_launch.h"

@@ -117,8 +117,6 @@ def load() -> ctypes.CDLL:
     lib.fa_get_wait_timeout_ns.argtypes = []
     lib.fa_debug_wait_timeout.restype = ctypes.c_int
     lib.fa_debug_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
-    lib.fa_debug_exp2.restype = ctypes.c_int
-    lib.fa_debug_exp2.argtypes = [vp, vp, vp, i32, vp]
     lib.fa_debug_softcap.restype = ctypes.c_int
     lib.fa_debug_softcap.argtypes = [vp, vp, i32, ctypes.c_float, vp]
     lib.fa_debug_tc5_gemm.restype = ctypes.c_int
@@ -462,14 +460,6 @@ def get_wait_timeout_ns() -> int:
 
 def debug_wait_timeout(status: torch.Tensor, timeout_ns: int) -> int:
     return int(load().fa_debug_wait_timeout(_ptr(status), int(timeout_ns), _stream(status.device)))
-
-
-def debug_exp2(x: torch.Tensor):
-    """(2^x by the FMA-pipe polynomial, 2^x by ex2.approx) for a contiguous fp32 CUDA tensor."""
-    yp = torch.empty_like(x)
-    ym = torch.empty_like(x)
-    _check(load().fa_debug_exp2(_ptr(x), _ptr(yp), _ptr(ym), x.numel(), _stream(x.device)), "fa_debug_exp2")
-    return yp, ym
 
 
 def debug_softcap(x: torch.Tensor, c: float) -> torch.Tensor:

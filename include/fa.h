@@ -85,7 +85,10 @@ typedef struct {
   int64_t arg[FA_MAX_RULE_OPS];    /* W for FA_M_WINDOW, P for FA_M_PREFIX, ignored otherwise */
   const int32_t* doc_ids;          /* device int32 [doc_batch, doc_len]; required iff a FA_M_DOC op */
   int32_t doc_batch;               /* 1 (one sequence layout for all b) or B */
-  int32_t doc_len;                 /* must cover every global position read on both sides */
+  int32_t doc_len;                 /* >= KV_LEN (every key position; else FA_ERR_SHAPE). A global query
+                                      position outside [0, doc_len) (reachable through q_offset or
+                                      Q_LEN > doc_len) reads as id -1: it shares a document with exactly
+                                      the keys whose id is -1 (none when all ids are >= 0) */
   const int32_t* q_offset;         /* device int32 [B] or NULL (= all zero) */
   int32_t batch_dependent;         /* 0: table broadcast over b (Bm = 1); 1: Bm = B */
   int32_t head_dependent;          /* 0: table broadcast over h (Hm = 1); 1: Hm = H */
@@ -302,9 +305,15 @@ FA_API fa_status fa_flex_decode(const void* q, const void* k_pages, const void* 
  * minus the workspace) and keeps the per-split state in one file-scope device array of
  * FA_DECODE_NOALLOC_SCRATCH_BYTES bytes that every GPU loading libfa.so holds until the process exits.
  *  - Set-up: the first call on a device, with that device current, looks up the array's device address
- *    (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any stream capture. A
+ *    cudaDeviceReset (or any other teardown of the device's context) invalidates the cached address
+ *    without the library noticing: do not use this entry point on a device after resetting it.
  *  - Size limit: a problem whose fa_decode_workspace_bytes(...) exceeds the array returns
  *    FA_ERR_BUFFER_TOO_SMALL and launches nothing (fa_decode_noalloc_scratch_bytes() reports the size).
+ *    Every other argument is checked first, with the codes fa_flex_decode returns for it. The need is
+ *    about Bz * Hq * n_splits * (d + 3) * 4 bytes, n_splits = ceil(max_pages / min(max_pages,
+ *    2048 / page)): with d = 128, 128-token pages, a 32768-token table (16 splits) and Hq = 32, up to 125
+ *    requests fit.
  *  - Sharing: all calls use the same array. Calls that overlap on the GPU (different streams with no
  *    ordering between them) race on it; calls on one stream are fine. Nothing in it needs clearing
  *    between calls.
@@ -344,11 +353,6 @@ FA_API fa_status fa_debug_wait_timeout(int32_t* dev_status, uint64_t timeout_ns,
  * shared memory. Used by the tests to pin the shared-memory, tensor-memory and instruction descriptors. */
 FA_API fa_status fa_debug_tc5_gemm(const void* A, const void* B, float* C, int32_t K, int32_t b_mn_major,
                             int32_t use_tma, int32_t* dev_status, fa_stream_t stream);
-
-/* Self-test of the two exponentials the forward kernel mixes: y_poly[i] = 2^x[i] from the FMA-pipe
- * polynomial (range reduction + cubic, max relative error 7.5e-5), y_mufu[i] = 2^x[i] from ex2.approx.
- * x, y_poly, y_mufu: device fp32 [n]. */
-FA_API fa_status fa_debug_exp2(const float* x, float* y_poly, float* y_mufu, int32_t n, fa_stream_t stream);
 
 /* Self-test of the soft-cap every kernel applies: y[i] = c * tanh(x[i] / c) ("5.1.2 FlexAttention: from
  * rules to fused kernels", section 1.2). x, y: device fp32 [n]; c > 0. */

@@ -18,6 +18,8 @@ What the oracle computes (exact attention restricted to the mask, [FA] Q8; [FX] 
   s_ij <- -inf where not A                     (mask after score_mod)                  ([FX] 1.2, 3.1)
   two-pass softmax: m = max_j s_ij, l = sum_j e^(s_ij - m), O = sum_j e^(s_ij - m)/l * v_j, LSE = m + ln l
   empty row (m = -inf): O = 0, LSE = -inf                                              ([K5] section 3)
+  document id of position t: doc_ids[b][t] for t in [0, doc_len), -1 outside, so a query position pushed
+  past the id array by an offset shares a document only with keys whose id is -1       ([FX] 1.1 reading)
 BlockMask tables ([FX] 2.1-2.2; [K5] section 4): per (b_m, h_m, query block r, KV block c) count the allowed
 pairs over the full Bq x Bk footprint: 0 -> empty, Bq*Bk -> full, otherwise partial (pairs outside
 [0,Q_LEN) x [0,KV_LEN) count as not allowed). Partial and full column lists per row, ascending, unused
@@ -211,11 +213,18 @@ def attention_rows(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, rule, rows:
     rows = np.asarray(rows, dtype=np.int64)
     j = np.arange(kv_len, dtype=np.int64)
     a = dense_allowed(rule, b, rows, q_len, kv_len, q_offset, doc_ids)
+    if not return_p:
+        # A key that no row of this call may see contributes exactly zero to every row (its score becomes
+        # -inf, e^-inf = 0: [FX] 1.2, [K5] 3), so its dot products are skipped; the rule was still
+        # evaluated on every pair above.
+        used = np.nonzero(a.any(axis=0))[0]
+        if used.size < kv_len:
+            j, a, k, v = j[used], a[:, used], k[used], v[used]
     s = scale * (q_rows @ k.T)
     s = score_mod(s, h, rows[:, None] + int(q_offset), j[None, :], score,
                   kv_len if bias_kv_len is None else bias_kv_len)
     s = np.where(a, s, -np.inf)
-    m = s.max(axis=1) if kv_len else np.full(len(rows), -np.inf)
+    m = s.max(axis=1) if s.shape[1] else np.full(len(rows), -np.inf)
     empty = ~np.isfinite(m)
     m_safe = np.where(empty, 0.0, m)
     p = np.exp(s - m_safe[:, None])                # exp(-inf) = 0 for masked pairs

@@ -56,37 +56,34 @@ def run_prefill(w: workloads.Prefill, force_mma=False, counters=False, bq=None, 
     return dict(out=out, lse=lse, bm=bm, status=st, counters=cnt, keep=(al, rb, doc, q, k, v))
 
 
-def sample_rows(w: workloads.Prefill, n_heads=3, rows_per_block=4, n_blocks=6, seed=0):
-    """Seeded sample: a few (b, h) pairs (first, last, random) and query rows from the first, the last and
-    random query blocks (always including each sampled block's first and last row)."""
+def sample_rows_every_block(w: workloads.Prefill, seed=0):
+    """Seeded rows for the full-size comparison: from EVERY query block, its first and last row and one
+    random row in between (every block of the prefill workloads holds a partial block: the diagonal)."""
     rng = np.random.default_rng(seed)
-    pairs = {(0, 0), (w.B - 1, w.Hq - 1)}
-    while len(pairs) < min(n_heads, w.B * w.Hq):
-        pairs.add((int(rng.integers(w.B)), int(rng.integers(w.Hq))))
     nq = -(-w.q_len // w.bq)
-    blocks = {0, nq - 1}
-    while len(blocks) < min(n_blocks, nq):
-        blocks.add(int(rng.integers(nq)))
-    rows = set()
-    for r in blocks:
+    per_block = []
+    for r in range(nq):
         lo, hi = r * w.bq, min(w.q_len, (r + 1) * w.bq)
-        rows.update({lo, hi - 1})
-        rows.update(int(x) for x in rng.integers(lo, hi, size=rows_per_block))
-    return sorted(pairs), np.array(sorted(rows), dtype=np.int64)
+        per_block.append(sorted({lo, hi - 1, int(rng.integers(lo, hi))}))
+    return per_block
 
 
-def oracle_rows(w: workloads.Prefill, pairs, rows):
-    """fp64 oracle O/LSE for the sampled (b, h) pairs and query rows."""
+def oracle_rows_per_block(w: workloads.Prefill, b: int, h: int, per_block):
+    """fp64 oracle O/LSE of one (b, h) for the rows of `per_block` (one oracle call per query block, so the
+    keys no sampled row of the block may see drop out of its dot products)."""
     g = w.Hq // w.Hkv
-    res = {}
-    for b, h in pairs:
-        hk = h // g
+    hk = h // g
+    kf = synth.bf16_bits_to_f64(w.k_bits[b, hk])
+    vf = synth.bf16_bits_to_f64(w.v_bits[b, hk])
+    sc = oracle_score(w.score)
+    os_, ls_ = [], []
+    for rows in per_block:
+        rows = np.asarray(rows, dtype=np.int64)
         qf = synth.bf16_bits_to_f64(w.q_bits[b, h, rows])
-        kf = synth.bf16_bits_to_f64(w.k_bits[b, hk])
-        vf = synth.bf16_bits_to_f64(w.v_bits[b, hk])
-        res[(b, h)] = orc.attention_rows(qf, kf, vf, w.rule, rows, b, h, w.q_len, w.kv_len, w.scale,
-                                         oracle_score(w.score), 0, w.doc_ids)
-    return res
+        o, l = orc.attention_rows(qf, kf, vf, w.rule, rows, b, h, w.q_len, w.kv_len, w.scale, sc, 0, w.doc_ids)
+        os_.append(o)
+        ls_.append(l)
+    return np.concatenate(os_), np.concatenate(ls_)
 
 
 def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
@@ -101,8 +98,8 @@ def compare(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: 
     """Tolerance check: max/mean |O - O*| and max |LSE - LSE*| (empty rows: LSE both -inf, O both 0).
 
     fp32 output: the bounds apply as stated. bf16 output: the stored value also carries the rounding of
-    the result to bf16, at most half an ulp of O*, which is added to the bound element by element (the
-    max bound alone is below that rounding for |O*| >= 4)."""
+    the result to bf16, at most half an ulp of O*, which is added to the max bound element by element (the
+    max bound alone is below that rounding for |O*| >= 4); the mean bound stays 1e-3 as stated."""
     err = np.abs(o_gpu.astype(np.float64) - o_ref)
     slack = half_ulp_bf16(o_ref) if out_bf16 else np.zeros_like(o_ref)
     inf_ref = np.isneginf(lse_ref)
@@ -110,7 +107,7 @@ def compare(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: 
     lerr = np.abs(lse_gpu[~inf_ref].astype(np.float64) - lse_ref[~inf_ref]) if (~inf_ref).any() else np.zeros(1)
     assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite output"
     assert np.all(err <= O_MAX + slack), f"{what}: max |O err| {err.max():.3e} (excess {(err - slack).max():.3e})"
-    assert err.mean() <= O_MEAN + slack.mean(), f"{what}: mean |O err| {err.mean():.3e}"
+    assert err.mean() <= O_MEAN, f"{what}: mean |O err| {err.mean():.3e}"
     assert lerr.max() <= LSE_MAX, f"{what}: max |LSE err| {lerr.max():.3e}"
     return float(err.max()), float(err.mean()), float(lerr.max())
 

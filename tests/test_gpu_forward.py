@@ -55,6 +55,11 @@ CASES = [
     ("bias_then_cap", 1, 2, 2, 150, 150, 64, 32, 32, [("causal",)],
      dict(alibi_slopes=np.array([0.05, 0.3], np.float32), softcap=5.0)),
     ("mqa_block16", 1, 4, 1, 96, 96, 128, 16, 128, CW(40), {}),
+    # more (batch, head pair) units than one group of eight, on the 128x128 path: the group order of the
+    # tcgen05 kernel (two tiles per CTA; one tile per CTA for the MHA window) is checked on every element
+    ("causal_9_pairs", 3, 6, 6, 384, 384, 128, 128, 128, [("causal",)], {}),
+    ("gqa_12_pairs_softcap", 2, 12, 4, 384, 384, 128, 128, 128, CW(200), dict(softcap=30.0)),
+    ("window_mha_10_heads", 2, 5, 5, 512, 512, 128, 128, 128, CW(256), {}),
 ]
 
 
@@ -104,17 +109,22 @@ def test_cfg1_all_elements(name):
 
 @pytest.mark.parametrize("name", ["cfg2", "cfg3", "cfg4"])
 def test_full_size_sampled(name):
+    # the launch configuration the benchmark times (fp32 O); every (b, h) pair, and from every query block
+    # (each holds a partial block) its first, last and one random row
     w = {"cfg2": workloads.cfg2, "cfg3": workloads.cfg3, "cfg4": workloads.cfg4}[name]().generate()
     r = gc.run_prefill(w, counters=True)
     assert r["status"] == fa.OK
-    pairs, rows = gc.sample_rows(w, seed=11)
-    ref = gc.oracle_rows(w, pairs, rows)
+    per_block = gc.sample_rows_every_block(w, seed=11)
+    rows = np.concatenate([np.asarray(x, dtype=np.int64) for x in per_block])
     out, lse = r["out"], r["lse"]
-    for (b, h), (o_ref, lse_ref) in ref.items():
-        assert out.dtype == torch.float32
-        o = out[b, h, torch.from_numpy(rows).cuda()].float().cpu().numpy()
-        l = lse[b, h, torch.from_numpy(rows).cuda()].cpu().numpy()
-        gc.compare(o, l, o_ref, lse_ref, f"{name} b={b} h={h}")
+    assert out.dtype == torch.float32
+    ridx = torch.from_numpy(rows).cuda()
+    o_all = out[:, :, ridx].cpu().numpy()
+    l_all = lse[:, :, ridx].cpu().numpy()
+    for b in range(w.B):
+        for h in range(w.Hq):
+            o_ref, lse_ref = gc.oracle_rows_per_block(w, b, h, per_block)
+            gc.compare(o_all[b, h], l_all[b, h], o_ref, lse_ref, f"{name} b={b} h={h}")
     # counters: one K and one V tile load per visited block, nothing for empty blocks
     st = fa.block_mask_stats(r["bm"]).cpu().tolist()
     c = r["counters"].cpu().tolist()
@@ -128,13 +138,11 @@ def test_full_size_sampled(name):
     assert np.all(np.isfinite(out.float().cpu().numpy()))
 
 
-def test_tc5_matches_mma_kernel_cfg2_small():
+def test_tc5_and_mma_kernels_cfg2_small_against_oracle():
+    # both kernels on a reduced cfg2 (B=1, H=4, N=1024), every element against the oracle
     w = workloads.cfg2(B=1, H=4, n=1024).generate()
-    a = gc.run_prefill(w)
-    b = gc.run_prefill(w, force_mma=True)
-    d = (a["out"].float() - b["out"].float()).abs().max().item()
-    assert d <= 8e-3
-    assert (a["lse"] - b["lse"]).abs().max().item() <= 2e-3
+    full_compare(w, what="cfg2 small tcgen05")
+    full_compare(w, force_mma=True, what="cfg2 small mma.sync")
 
 
 @pytest.mark.parametrize("kind", ["causal_mha", "gqa_docs_per_batch_alibi", "head_dependent_window_bf16"])
