@@ -461,7 +461,9 @@ __global__ void __launch_bounds__(Roles<NT>::kThreads, Roles<NT>::kCtasPerSm)
       if (SK == SK_ALIBI || SK == SK_GENERIC) slope2 = a.score.alibi ? __ldg(a.score.alibi + TT.h) * kLog2e : 0.f;
       const int c_lo = 64 * h;                 // first column of this half within the block
       float m_ref = -INFINITY;  // reference max (log2 domain) used for P and for O
-      float l = 0.f, le = 0.f;  // this half's row sums (rounded P for O, unrounded P for the LSE)
+      // this half's row sum of P (for the LSE), and the correction that turns it into the sum O is divided
+      // by: per block, the bf16 rounding error of the half's largest P (see the P loop)
+      float le = 0.f, lc = 0.f;
       bool ok = true;
       // tcgen05.ld / st are warp-collective (.sync.aligned): every decision that guards one is made
       // uniform across the warp (wait results with __all_sync, the O rescale with __any_sync). The
@@ -545,7 +547,8 @@ __global__ void __launch_bounds__(Roles<NT>::kThreads, Roles<NT>::kCtasPerSm)
         for (int i = 8; i < 64; i += 8)
 #pragma unroll
           for (int k = 0; k < 4; ++k) mxk[k] = fmax3(mxk[k], x[i + k], x[i + 4 + k]);
-        s_red[t][h][row] = fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3])) * mult;
+        const float hmax = fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3]));
+        s_red[t][h][row] = hmax * mult;
         named_bar_sync(1 + t, 256);
         const float mb = fmaxf(s_red[t][0][row], s_red[t][1][row]);
         // ---- reference max: move it only when the block max exceeds it by more than 2^8
@@ -557,11 +560,14 @@ __global__ void __launch_bounds__(Roles<NT>::kThreads, Roles<NT>::kCtasPerSm)
           m_ref = mb;
         }
         const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-        // ---- P = 2^(mult * x - m); two row sums: of the bf16-rounded P the product uses (normalises O:
-        // an exact convex combination of V rows) and of the unrounded P (for the LSE). P is stored 16
-        // columns (32 keys) at a time.
+        // ---- P = 2^(mult * x - m), stored as bf16 16 columns (32 keys) at a time, and the row sum of the
+        // unrounded P. The product multiplies the bf16-rounded P; O is divided by the unrounded sum plus, per
+        // block, the rounding error of this half's largest P (the same FMA and ex2 on the same input give
+        // that element's P bit for bit). A row dominated by one key then gets that key's V row with an exact
+        // weight, as if O were divided by the sum of the rounded values; what is left is the rounding of
+        // the smaller weights, at most 2^-9 of their share.
         const uint64_t mul2 = f2_pack(mult, mult), neg2 = f2_pack(-mr, -mr);
-        uint64_t se[2] = {0, 0}, sr[2] = {0, 0};
+        uint64_t se[2] = {0, 0};
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
           uint32_t pk[16];
@@ -572,15 +578,15 @@ __global__ void __launch_bounds__(Roles<NT>::kThreads, Roles<NT>::kCtasPerSm)
             const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
             pk[i] = pack_bf16x2(p0, p1);
             se[i & 1] = f2_add(se[i & 1], f2_pack(p0, p1));
-            sr[i & 1] = f2_add(sr[i & 1], f2_pack(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xFFFF0000u)));
           }
           tc5_st16(tS + c_lo + 16 * ch, pk);
         }
-        float e0, e1, r0, r1;
+        const float ph = ex2_approx(fmaf(hmax, mult, -mr));
+        const float ch_err = __uint_as_float(pack_bf16x2(ph, 0.f) << 16) - ph;
+        float e0, e1;
         f2_unpack(f2_add(se[0], se[1]), e0, e1);
-        f2_unpack(f2_add(sr[0], sr[1]), r0, r1);
-        l = l * alpha + (r0 + r1);
         le = le * alpha + (e0 + e1);
+        lc = lc * alpha + ch_err;
         // ---- O is stable here: S_t(j) completed, and O_t's previous update was issued before it.
         // Each half rescales its half of O's columns.
         if (__any_sync(0xFFFFFFFFu, rescale)) {
@@ -605,7 +611,7 @@ __global__ void __launch_bounds__(Roles<NT>::kThreads, Roles<NT>::kCtasPerSm)
       tc5_fence_after();
       // the last O update completed after both halves read the last block's maxima: the exchange
       // buffer is free for the two sums, one at a time
-      s_red[t][h][row] = l;
+      s_red[t][h][row] = le + lc;
       named_bar_sync(1 + t, 256);
       const float lt = s_red[t][0][row] + s_red[t][1][row];
       named_bar_sync(1 + t, 256);

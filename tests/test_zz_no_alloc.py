@@ -67,17 +67,27 @@ def test_noalloc_decode_matches_workspace_decode_twice(out_dtype):
 
 
 def test_noalloc_decode_refuses_oversized_problems():
+    # A problem whose split workspace exceeds the fixed array, with every other argument valid: a table
+    # shared by all requests (no per-request state, Bm = 1) declared for a batch far larger than the array
+    # can hold. fa_flex_decode checks all other arguments first, so the refusal is the size, and nothing is
+    # launched (the batch is never touched).
     dec = workloads.cfg5(Bz=2, Hq=4, Hkv=2, d=64, page=32, lo=40, hi=200).generate()
-    q, kp, vp, pt, bm = _setup(dec)
-    # same pages and table, but declared for a batch far larger than the fixed array can hold
+    q, kp, vp, pt, _ = _setup(dec)
+    shared = fa.create_block_mask(fa.make_mask_rule([("causal",)]), 1, dec.Hq, 1, dec.kv_len, 1, dec.page)
     big_bz = 1 << 17
     assert fa.decode_workspace_bytes(big_bz, dec.Hq, dec.d, dec.max_pages, dec.page) > \
         fa.decode_noalloc_scratch_bytes()
     lib = fa.load()
     out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
     lse = torch.empty((dec.Bz, dec.Hq), dtype=torch.float32, device="cuda")
-    code = lib.fa_flex_decode_noalloc(fa._ptr(q), fa._ptr(kp), fa._ptr(vp), fa._ptr(pt), kp.shape[0],
-                                      fa.ctypes.byref(bm.c), None, 0.0, fa._ptr(out), 1, fa._ptr(lse), big_bz,
-                                      dec.Hq, dec.Hkv, dec.d, dec.page, dec.max_pages, None, None,
-                                      fa._stream(q.device))
-    assert code == fa.ERR_BUFFER
+
+    def call(bz, d):
+        return lib.fa_flex_decode_noalloc(fa._ptr(q), fa._ptr(kp), fa._ptr(vp), fa._ptr(pt), kp.shape[0],
+                                          fa.ctypes.byref(shared.c), None, 0.0, fa._ptr(out), 1, fa._ptr(lse), bz,
+                                          dec.Hq, dec.Hkv, d, dec.page, dec.max_pages, None, None,
+                                          fa._stream(q.device))
+
+    assert call(big_bz, dec.d) == fa.ERR_BUFFER
+    # another argument error in the same call keeps the code fa_flex_decode gives it
+    assert call(big_bz, 96) == fa.ERR_UNSUPPORTED
+    torch.cuda.synchronize()
