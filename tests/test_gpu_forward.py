@@ -125,16 +125,15 @@ def test_full_size_sampled(name):
         for h in range(w.Hq):
             o_ref, lse_ref = gc.oracle_rows_per_block(w, b, h, per_block)
             gc.compare(o_all[b, h], l_all[b, h], o_ref, lse_ref, f"{name} b={b} h={h}")
-    # counters: one K and one V tile load per visited block, nothing for empty blocks
+    # counters: every visited block of every tile counted once; a CTA's two tiles read one KV head and load
+    # each block of the union of their lists once (K and V), so the loads lie between one and two per
+    # visited tile-block
     st = fa.block_mask_stats(r["bm"]).cpu().tolist()
     c = r["counters"].cpu().tolist()
     heads = w.B * w.Hq // (r["bm"].c.Bm * r["bm"].c.Hm)
     assert c[1] == st[0] * heads and c[2] == st[1] * heads
-    # one K and one V load per visited block; the tcgen05 kernel shares them between the two query
-    # tiles of a CTA when both heads read the same KV head through the same mask row (GQA)
-    g = w.Hq // w.Hkv
-    shared = w.bq == 128 and w.bk == 128 and g >= 2 and w.Hq % 2 == 0 and r["bm"].c.Hm == 1
-    assert c[3] == (1 if shared else 2) * (c[1] + c[2])
+    visited = c[1] + c[2]
+    assert visited <= c[3] <= 2 * visited
     assert np.all(np.isfinite(out.float().cpu().numpy()))
 
 
