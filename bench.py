@@ -42,6 +42,7 @@ def parse():
     p.add_argument("--no-backward", action="store_true")
     p.add_argument("--no-paged", action="store_true")
     p.add_argument("--no-others", action="store_true", help="skip the other prefill workloads")
+    p.add_argument("--no-split", action="store_true", help="skip the split-row prefill line")
     p.add_argument("--backward-only", action="store_true",
                    help="after the forward, time only the backward and print its object as the line (profiling aid)")
     return p.parse_args()
@@ -523,6 +524,12 @@ def ours(args, rank, world, local_rank):
                 others[name] = other_prefill(name, args, dev, pk, world)
                 torch.cuda.empty_cache()
 
+    # ---------------- split rows: a chunked prefill over a long context, with and without splitting its rows
+    split_line = None
+    if not args.no_split:
+        split_line = bench_split_prefill(args, dev, pk)
+        torch.cuda.empty_cache()
+
     # ---------------- decode (secondary metric of the same hot path): paged split-KV, 64 requests
     dec_line = None
     if not args.no_decode:
@@ -560,6 +567,8 @@ def ours(args, rank, world, local_rank):
     })
     if others:
         line["prefill_workloads"] = others
+    if split_line:
+        line["split_prefill"] = split_line
     if dec_line:
         line["decode"] = dec_line
     if bwd_line:
@@ -628,6 +637,44 @@ def time_events(fn, n, stream):
         b.record(stream)
     torch.cuda.synchronize()
     return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def bench_split_prefill(args, dev, pk, q_len=256, kv_len=131072, H=8, chunk=64):
+    """fa_flex_forward_split against fa_flex_forward on a chunked prefill: q_len new tokens at the end of a
+    kv_len-token context (causal in global positions, query offset kv_len - q_len), B = 1, Hq = Hkv = H,
+    d = 128, 128 x 128 blocks. Unsplit, each CTA walks two whole rows of ~kv_len / 128 key blocks and only
+    H * ceil(q_len / 256) CTAs exist; split into chunks of `chunk` key blocks, the rows spread over the GPU."""
+    import numpy as np
+    import torch
+
+    from block_sparse_masked_create_gb300 import fa, workloads
+    w = workloads.Prefill("chunked_prefill", 1, H, H, q_len, kv_len, 128, 128, 128, [("causal",)], {},
+                          1.0 / math.sqrt(128), 0x5EED0010).generate()
+    q = workloads.bf16_torch(w.q_bits, dev)
+    k = workloads.bf16_torch(w.k_bits, dev)
+    v = workloads.bf16_torch(w.v_bits, dev)
+    off = torch.tensor([kv_len - q_len], dtype=torch.int32, device=dev)
+    rule = fa.make_mask_rule(w.rule, q_offset=off, batch_dependent=True)
+    bm = fa.create_block_mask(rule, 1, H, q_len, kv_len, 128, 128, device=dev, keep=[off])
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty((1, H, q_len), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.forward_split_workspace_bytes(bm, 1, H, 128, chunk), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = fa.block_mask_stats(bm).cpu().tolist()
+    flop = 4.0 * 128 * 128 * 128 * (st[0] + st[1]) * H
+    stream = torch.cuda.current_stream(dev)
+    steps = max(5, args.steps)
+    ms_plain = time_events(lambda: fa.flex_forward(q, k, v, bm, None, w.scale, out=out, lse=lse, status=status),
+                           steps, stream)
+    ms_split = time_events(lambda: fa.flex_forward_split(q, k, v, bm, None, w.scale, chunk_blocks=chunk, out=out,
+                                                         lse=lse, workspace=ws, status=status), steps, stream)
+    tf_split = flop / (ms_split * 1e-3) / 1e12
+    return {"workload": f"chunked prefill: {q_len} new tokens after a {kv_len - q_len}-token context, B=1 "
+                        f"Hq=Hkv={H} d=128, causal in global positions, 128x128 blocks; chunks of {chunk} key blocks",
+            "rows_max_blocks": st[3], "forward_ms_median": ms_plain, "split_ms_median": ms_split,
+            "forward_tflops": flop / (ms_plain * 1e-3) / 1e12, "split_tflops": tf_split,
+            "split_pct_bf16_peak": tf_split / pk["bf16"], "speedup": ms_plain / ms_split,
+            "launches_split": 3, "status": fa.status_string(fa.check_status(status))}
 
 
 def bench_paged_prefill(args, dev, pk, w, q, bm, sc, phys_flops):

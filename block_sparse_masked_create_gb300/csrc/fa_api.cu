@@ -245,11 +245,21 @@ struct PagedKV {  // all zero: contiguous K / V
   int32_t n_pages_total, page, max_pages;
 };
 
+// Split rows: the derived tables (entries e = r * ncm + c) and the per-entry outputs the forward writes
+// instead of O and LSE.
+struct SplitPlan {
+  DevMask mask;
+  int32_t ncm;
+  float* o_part;    // fp32 [B, Hq, nq * ncm * 128, d]
+  float* lse_part;  // fp32 [B, Hq, nq * ncm * 128]
+};
+
 static int forward_impl(bool force_mma, const void* q, const void* k, const void* v, const fa_block_mask* bm,
                         const fa_score_rule* score, float scale, void* out, int32_t out_dtype, float* lse,
                         int32_t B, int32_t Hq,
                         int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d, int32_t* dev_status,
-                        int64_t* dev_counters, fa_stream_t stream, const PagedKV& pg = PagedKV{}) {
+                        int64_t* dev_counters, fa_stream_t stream, const PagedKV& pg = PagedKV{},
+                        const SplitPlan* split = nullptr) {
   int s = check_forward(q, k, v, bm, out, lse, B, Hq, Hkv, Q_LEN, KV_LEN, d);
   if (s != FA_OK) return s;
   if (out_dtype != FA_OUT_BF16 && out_dtype != FA_OUT_F32) return FA_ERR_INVALID_ARG;
@@ -284,7 +294,18 @@ static int forward_impl(bool force_mma, const void* q, const void* k, const void
   a.page_table = pg.page_table;
   a.max_pages = pg.max_pages;
   a.n_pages_total = pg.n_pages_total;
+  a.split_ncm = 1;
+  a.out_q_len = Q_LEN;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (split) {  // the tcgen05 kernel over the derived tables, writing each entry's O and LSE
+    a.mask = split->mask;
+    a.split_ncm = split->ncm;
+    a.out_q_len = split->mask.nq * 128;
+    a.out = split->o_part;
+    a.out_f32 = 1;
+    a.lse = split->lse_part;
+    return launch_fwd_tc5(a, st);
+  }
   if (!force_mma && bm->bq == 128 && bm->bk == 128) {
     int r = launch_fwd_tc5(a, st);
     if (r != FA_ERR_UNSUPPORTED) return r;
@@ -784,6 +805,104 @@ fa_status fa_flex_decode(const void* q, const void* k_pages, const void* v_pages
   a.counters = dev_counters;
   a.timeout_ns = g_timeout_ns.load();
   return (fa_status)launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------------------------------------
+// Split rows ("5 Kernels ...", section 5)
+// ------------------------------------------------------------------------------------------------
+struct SplitLayout {
+  int ncm;
+  size_t nqd, off_num, off_fnum, off_order, off_idx, off_fidx, off_o, off_lse, total;
+};
+
+static bool split_layout(const fa_block_mask* bm, int32_t B, int32_t Hq, int32_t d, int32_t C, SplitLayout* L) {
+  if (!bm || B < 1 || Hq < 1 || d < 1 || C < 1 || bm->nq < 1 || bm->nk < 1) return false;
+  L->ncm = (bm->nk + C - 1) / C;
+  L->nqd = (size_t)bm->nq * L->ncm;
+  if (L->nqd * 128 > (size_t)INT_MAX) return false;
+  const size_t bh = (size_t)bm->Bm * bm->Hm, rows = (size_t)B * Hq * L->nqd * 128;
+  size_t o = 0;
+  L->off_num = o;   o += align256(bh * L->nqd * 4);
+  L->off_fnum = o;  o += align256(bh * L->nqd * 4);
+  L->off_order = o; o += align256(bh * L->nqd * 4);
+  L->off_idx = o;   o += align256(bh * L->nqd * C * 4);
+  L->off_fidx = o;  o += align256(bh * L->nqd * C * 4);
+  L->off_o = o;     o += align256(rows * d * 4);
+  L->off_lse = o;   o += align256(rows * 4);
+  L->total = o;
+  return true;
+}
+
+size_t fa_forward_split_workspace_bytes(const fa_block_mask* bm, int32_t B, int32_t Hq, int32_t d,
+                                        int32_t chunk_blocks) {
+  SplitLayout L;
+  return split_layout(bm, B, Hq, d, chunk_blocks, &L) ? L.total : 0;
+}
+
+fa_status fa_flex_forward_split(const void* q, const void* k, const void* v, const fa_block_mask* bm,
+                                const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype,
+                                float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN,
+                                int32_t d, int32_t chunk_blocks, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, fa_stream_t stream) {
+  int s = check_forward(q, k, v, bm, out, lse, B, Hq, Hkv, Q_LEN, KV_LEN, d);
+  if (s != FA_OK) return (fa_status)s;
+  if (out_dtype != FA_OUT_BF16 && out_dtype != FA_OUT_F32) return FA_ERR_INVALID_ARG;
+  if (bm->bq != 128 || bm->bk != 128) return FA_ERR_UNSUPPORTED;
+  if (chunk_blocks < 1 || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FA_ERR_INVALID_ARG;
+  SplitLayout L;
+  if (!split_layout(bm, B, Hq, d, chunk_blocks, &L)) return FA_ERR_SHAPE;
+  if (workspace_bytes < L.total) return FA_ERR_BUFFER_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  MaskOut S;
+  std::memset(&S, 0, sizeof(S));
+  S.Bm = bm->Bm;
+  S.Hm = bm->Hm;
+  S.nq = bm->nq;
+  S.nk = bm->nk;
+  S.kv_num = bm->kv_num;
+  S.kv_idx = bm->kv_idx;
+  S.full_kv_num = bm->full_kv_num;
+  S.full_kv_idx = bm->full_kv_idx;
+  MaskOut D;
+  std::memset(&D, 0, sizeof(D));
+  D.Bm = bm->Bm;
+  D.Hm = bm->Hm;
+  D.q_len = Q_LEN;
+  D.kv_len = KV_LEN;
+  D.bq = D.bk = 128;
+  D.nq = (int32_t)L.nqd;
+  D.nk = chunk_blocks;  // row stride of the derived lists
+  D.kv_num = reinterpret_cast<int32_t*>(w + L.off_num);
+  D.full_kv_num = reinterpret_cast<int32_t*>(w + L.off_fnum);
+  D.row_order = reinterpret_cast<int32_t*>(w + L.off_order);
+  D.kv_idx = reinterpret_cast<int32_t*>(w + L.off_idx);
+  D.full_kv_idx = reinterpret_cast<int32_t*>(w + L.off_fidx);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_mask_split(S, chunk_blocks, L.ncm, D, st) != cudaSuccess) return FA_ERR_CUDA;
+  SplitPlan P;
+  std::memset(&P, 0, sizeof(P));
+  P.mask.Bm = D.Bm;
+  P.mask.Hm = D.Hm;
+  P.mask.q_len = Q_LEN;
+  P.mask.kv_len = KV_LEN;
+  P.mask.bq = P.mask.bk = 128;
+  P.mask.nq = D.nq;
+  P.mask.nk = D.nk;
+  P.mask.kv_num = D.kv_num;
+  P.mask.kv_idx = D.kv_idx;
+  P.mask.full_kv_num = D.full_kv_num;
+  P.mask.full_kv_idx = D.full_kv_idx;
+  P.mask.row_order = D.row_order;
+  P.ncm = L.ncm;
+  P.o_part = reinterpret_cast<float*>(w + L.off_o);
+  P.lse_part = reinterpret_cast<float*>(w + L.off_lse);
+  s = forward_impl(false, q, k, v, bm, score_rule, scale, out, out_dtype, lse, B, Hq, Hkv, Q_LEN, KV_LEN, d,
+                   dev_status, nullptr, stream, PagedKV{}, &P);
+  if (s != FA_OK) return (fa_status)s;
+  return launch_split_combine(P.o_part, P.lse_part, B, Hq, Q_LEN, bm->nq, L.ncm, d, out, out_dtype == FA_OUT_F32,
+                              lse, st) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
 }
 
 fa_status fa_block_mask_stats(const fa_block_mask* bm, int64_t* dev_out, fa_stream_t stream) {

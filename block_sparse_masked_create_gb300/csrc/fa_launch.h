@@ -65,6 +65,10 @@ struct FwdArgs {
   // and key block c of batch row b lives in page page_table[b * max_pages + c] (one page per key block)
   const int32_t* page_table;
   int32_t max_pages, n_pages_total;
+  // split rows (tcgen05 kernel only): the mask's rows are entries e = r * split_ncm + c, chunk c of query
+  // block r; Q and every position come from block e / split_ncm, while O (fp32) and LSE of entry e are
+  // written at rows e * 128 .. of [B, Hq, out_q_len]. split_ncm = 1 and out_q_len = q_len otherwise.
+  int32_t split_ncm, out_q_len;
 };
 
 cudaError_t launch_fwd_mma(const FwdArgs& a, cudaStream_t st);
@@ -123,6 +127,16 @@ cudaError_t launch_backward(const BwdArgs& a, cudaStream_t st);
 int launch_bwd_tc5(const BwdArgs& a, cudaStream_t st);
 
 cudaError_t launch_debug_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t st);
+
+// Split rows. From a BlockMask S (q_len rows of Bq = 128), the derived tables D: per (b_m, h_m) and
+// entry e = r * ncm + c, chunk c of block row r's visited blocks (full and partial merged in column
+// order, chunk = positions [c C, c C + C) of that order), as full / partial lists of row stride C; and a
+// row order that takes chunk c of every row (rows from the last) before chunk c + 1.
+cudaError_t launch_mask_split(const MaskOut& S, int C, int ncm, const MaskOut& D, cudaStream_t st);
+// Merge the entries of each query row (normalised O_e fp32 [B, Hq, nq * ncm * 128, d], LSE_e [B, Hq,
+// nq * ncm * 128]) into O (bf16 or fp32) [B, Hq, q_len, d] and LSE [B, Hq, q_len].
+cudaError_t launch_split_combine(const float* o_part, const float* lse_part, int B, int Hq, int q_len, int nq,
+                                 int ncm, int d, void* out, int out_f32, float* lse, cudaStream_t st);
 
 // Host helpers: encode a bf16 / fp32 tensor map (dims innermost first) with 128-byte swizzle.
 int encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,

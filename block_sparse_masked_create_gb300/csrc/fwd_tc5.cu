@@ -76,10 +76,11 @@ __device__ __forceinline__ uint32_t tile_off(int row, int c16) {
   return (uint32_t)((c16 >> 3) * 16384 + row * 128 + (((c16 & 7) ^ (row & 7)) << 4));
 }
 
-// One 128-row query tile: query head h (KV head hk), query block r, and its BlockMask row.
+// One 128-row query tile: query head h (KV head hk), BlockMask row r, and the query block rq it reads
+// (rq = r, or with split rows the block of entry r). O and LSE go to rows r * 128 .. of the output.
 struct Tile {
   int valid;     // a tile exists (Hq or the number of query blocks may be odd)
-  int h, hk, r;
+  int h, hk, r, rq;
   int n_full, n_part, n;
   const int32_t* full_idx;
   const int32_t* part_idx;
@@ -91,6 +92,7 @@ __device__ __forceinline__ Tile make_tile(const FwdArgs& a, int b, int h, int r)
   T.valid = h < a.Hq && r >= 0;
   T.h = T.valid ? h : 0;
   T.r = T.valid ? r : 0;
+  T.rq = a.split_ncm > 1 ? T.r / a.split_ncm : T.r;
   T.hk = T.h / (a.Hq / a.Hkv);
   const int bm = M.Bm > 1 ? b : 0, hm = M.Hm > 1 ? T.h : 0;
   const size_t mrow = ((size_t)bm * M.Hm + hm) * M.nq + T.r;
@@ -288,13 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx_elect(&bar_q[0], C::kQBytes);
 #pragma unroll
       for (int x = 0; x < D / 64; ++x)
-        tma_load_3d_elect(sQ0 + x * 16384, &tmQ, x * 64, T0.r * 128, b * a.Hq + T0.h, &bar_q[0]);
+        tma_load_3d_elect(sQ0 + x * 16384, &tmQ, x * 64, T0.rq * 128, b * a.Hq + T0.h, &bar_q[0]);
     }
     if (T1.n > 0) {
       mbar_arrive_expect_tx_elect(&bar_q[1], C::kQBytes);
 #pragma unroll
       for (int x = 0; x < D / 64; ++x)
-        tma_load_3d_elect(sQ1 + x * 16384, &tmQ, x * 64, T1.r * 128, b * a.Hq + T1.h, &bar_q[1]);
+        tma_load_3d_elect(sQ1 + x * 16384, &tmQ, x * 64, T1.rq * 128, b * a.Hq + T1.h, &bar_q[1]);
     }
     uw.init(T0, T1, desc);
     if (!uw.done()) {  // K of the first element (the ring has more slots than this)
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile Tn = make_tile(a, bn, tt ? hn1 : hn0, tt ? rn1 : rn0);
         if (Tn.n == 0) continue;
 #pragma unroll
-        for (int x = 0; x < D / 64; ++x) tma_prefetch_l2_3d(&tmQ, x * 64, Tn.r * 128, bn * a.Hq + Tn.h);
+        for (int x = 0; x < D / 64; ++x) tma_prefetch_l2_3d(&tmQ, x * 64, Tn.rq * 128, bn * a.Hq + Tn.h);
       }
     }
     __syncwarp();
@@ -466,21 +468,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool ring_stage = a.out_f32 && (single || same_list);
     const int slot_base = single ? 1 : (t ? 4 : 2);
     uint8_t* const sQt = t ? sQ1 : sQ0;
-    const int q_row = TT.r * 128 + row;
+    const int q_row = TT.rq * 128 + row;  // query position within the sequence (rule, score, validity)
+    const int o_row = TT.r * 128 + row;   // output row (the same unless rows are split)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::col_s(t);
     const uint32_t tO = tmem + lane_base + C::col_o(t);
-    float* Lg = a.lse + ((size_t)b * a.Hq + TT.h) * a.q_len;
+    float* Lg = a.lse + ((size_t)b * a.Hq + TT.h) * a.out_q_len;
     const bool issuer = (warp & 3) == 0 && lane == 0;
     if (TT.valid && TT.n == 0) {
-      // empty query block: O = 0, LSE = -inf, nothing loaded
+      // empty query block: O = 0, LSE = -inf, nothing loaded (an empty chunk of a split row only needs its
+      // LSE: the merge gives it no weight)
       const int row_bytes = D * (a.out_f32 ? 4 : 2);
-      uint8_t* Ob = reinterpret_cast<uint8_t*>(a.out) + (((size_t)b * a.Hq + TT.h) * a.q_len) * row_bytes;
+      uint8_t* Ob = reinterpret_cast<uint8_t*>(a.out) + (((size_t)b * a.Hq + TT.h) * a.out_q_len) * row_bytes;
       if (q_row < a.q_len) {
         const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int c16 = 0; c16 < row_bytes / 16; ++c16)
-          *reinterpret_cast<uint4*>(Ob + (size_t)q_row * row_bytes + c16 * 16) = z;
-        Lg[q_row] = -INFINITY;
+        if (a.split_ncm <= 1)
+          for (int c16 = 0; c16 < row_bytes / 16; ++c16)
+            *reinterpret_cast<uint4*>(Ob + (size_t)o_row * row_bytes + c16 * 16) = z;
+        Lg[o_row] = -INFINITY;
       }
     } else if (TT.valid) {
       const int64_t off_b = a.rule.q_offset ? (int64_t)__ldg(a.rule.q_offset + (M.Bm > 1 ? b : 0)) : 0;
@@ -640,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc5_fence_after();
       const bool empty = m_ref == -INFINITY;
       const float inv = empty ? 0.f : 1.f / (le + lc);
-      if (ok && q_row < a.q_len) Lg[q_row] = empty ? -INFINITY : (m_ref + __log2f(le)) * kLn2;
+      if (ok && q_row < a.q_len) Lg[o_row] = empty ? -INFINITY : (m_ref + __log2f(le)) * kLn2;
       // fp32 O ([128][D], D / 32 boxes of [128][32]: 128-byte rows, 128-byte swizzle) is staged in K / V
       // ring slots that no product reads any more and no load refills: with a single tile in use, its last
       // product is the CTA's last MMA and every slot is free then (it takes the slots of the last two
@@ -737,12 +742,15 @@ int launch_k(const FwdArgs& a, cudaStream_t st) {
   if (encode_tmap_bf16(&tq, a.q, 3, dq, sq, box) || encode_tmap_bf16(&tk, a.k, 3, dk, sk, box) ||
       encode_tmap_bf16(&tv, a.v, 3, dk, sk, box))
     return FA_ERR_CUDA;
+  // O: [B * Hq, out_q_len, D] (out_q_len = q_len unless rows are split)
+  const uint64_t dout[3] = {(uint64_t)D, (uint64_t)a.out_q_len, (uint64_t)a.B * a.Hq};
   if (a.out_f32) {
-    const uint64_t so[2] = {(uint64_t)D * 4, (uint64_t)a.q_len * D * 4};
+    const uint64_t so[2] = {(uint64_t)D * 4, (uint64_t)a.out_q_len * D * 4};
     const uint32_t boxo[3] = {32, 128, 1};
-    if (encode_tmap_f32(&to, a.out, 3, dq, so, boxo)) return FA_ERR_CUDA;
-  } else if (encode_tmap_bf16(&to, a.out, 3, dq, sq, box)) {
-    return FA_ERR_CUDA;
+    if (encode_tmap_f32(&to, a.out, 3, dout, so, boxo)) return FA_ERR_CUDA;
+  } else {
+    const uint64_t so[2] = {(uint64_t)D * 2, (uint64_t)a.out_q_len * D * 2};
+    if (encode_tmap_bf16(&to, a.out, 3, dout, so, box)) return FA_ERR_CUDA;
   }
   Tc5Params p;
   std::memset(&p, 0, sizeof(p));

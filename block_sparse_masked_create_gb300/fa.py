@@ -86,6 +86,11 @@ def load() -> ctypes.CDLL:
     lib.fa_block_mask_select_bytes.argtypes = [P(BlockMaskC), i32]
     lib.fa_block_mask_select_rows.restype = ctypes.c_int
     lib.fa_block_mask_select_rows.argtypes = [P(BlockMaskC), vp, i32, vp, sz, P(BlockMaskC), vp, vp]
+    lib.fa_forward_split_workspace_bytes.restype = sz
+    lib.fa_forward_split_workspace_bytes.argtypes = [P(BlockMaskC), i32, i32, i32, i32]
+    lib.fa_flex_forward_split.restype = ctypes.c_int
+    lib.fa_flex_forward_split.argtypes = [vp, vp, vp, P(BlockMaskC), P(ScoreRule), f32, vp, i32, vp, i32, i32, i32, i32,
+                                          i32, i32, i32, vp, sz, vp, vp]
     lib.fa_forward_host_workspace_bytes.restype = sz
     lib.fa_forward_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.fa_flex_forward_host.restype = ctypes.c_int
@@ -312,6 +317,39 @@ def flex_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: 
     _check(fn(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(block_mask.c), ctypes.byref(score) if score else None,
               float(scale) if scale else 0.0, _ptr(out), _out_code(out), _ptr(lse), B, Hq, Hkv, Q_LEN, KV_LEN, d,
               _ptr(status), _ptr(counters), _stream(q.device)), "fa_flex_forward")
+    return out, lse
+
+
+def forward_split_workspace_bytes(block_mask: BlockMask, B: int, Hq: int, d: int, chunk_blocks: int) -> int:
+    return int(load().fa_forward_split_workspace_bytes(ctypes.byref(block_mask.c), B, Hq, d, chunk_blocks))
+
+
+def flex_forward_split(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: BlockMask,
+                       score: Optional[ScoreRule] = None, scale: Optional[float] = None, chunk_blocks: int = 16,
+                       out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                       out_dtype=torch.bfloat16):
+    """fa_flex_forward_split: the forward with each query block row cut into chunks of at most chunk_blocks
+    key blocks, run as separate tiles and merged. Same inputs and outputs as flex_forward."""
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    B, Hq, Q_LEN, d = q.shape
+    Hkv, KV_LEN = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Q_LEN), dtype=torch.float32, device=q.device)
+    n = forward_split_workspace_bytes(block_mask, B, Hq, d, chunk_blocks)
+    if n == 0:
+        raise FaError(ERR_SHAPE, "fa_forward_split_workspace_bytes")
+    if workspace is None or workspace.numel() < n:
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    _check(load().fa_flex_forward_split(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(block_mask.c),
+                                        ctypes.byref(score) if score else None, float(scale) if scale else 0.0,
+                                        _ptr(out), _out_code(out), _ptr(lse), B, Hq, Hkv, Q_LEN, KV_LEN, d,
+                                        chunk_blocks, _ptr(workspace), workspace.numel(), _ptr(status),
+                                        _stream(q.device)), "fa_flex_forward_split")
     return out, lse
 
 

@@ -247,6 +247,31 @@ FA_API fa_status fa_flex_forward_paged(const void* q, const void* k_pages, const
                                        float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN,
                                        int32_t KV_LEN, int32_t d, int32_t* dev_status, fa_stream_t stream);
 
+/* The same forward with long rows split ("5 Kernels: turning logical sparsity into real speed-ups",
+ * section 5: a long row becomes several tasks, each with its own softmax state, merged once; the merge law
+ * of its section 3; "5.1.2 FlexAttention ...", section 5.2 on the long tail of row lengths). Each query
+ * block row's visited blocks, in column order, are cut into chunks of at most chunk_blocks blocks; every
+ * chunk runs as its own query tile (the tcgen05 kernel) and writes its normalised O and LSE to the
+ * workspace, and a second kernel merges the chunks of each row: with m = max_c LSE_c,
+ * O = sum_c e^(LSE_c - m) O_c / sum_c e^(LSE_c - m), LSE = m + ln sum_c e^(LSE_c - m) (an empty chunk has no
+ * weight; a row with no visited block gets O = 0, LSE = -inf). A row of up to chunk_blocks blocks is one
+ * chunk. The result equals fa_flex_forward's up to the summation order.
+ *   arguments as fa_flex_forward (no counters), plus
+ *   chunk_blocks   >= 1, key blocks per chunk
+ *   workspace      device buffer of >= fa_forward_split_workspace_bytes(block_mask, B, Hq, d, chunk_blocks)
+ *                  bytes, 256-byte aligned: the split tables and the per-chunk O (fp32) and LSE, about
+ *                  B * Hq * nq * ceil(nk / chunk_blocks) * 128 * (d + 1) * 4 bytes
+ * Supported: Bq == Bk == 128, d in {64, 128}. Returns the errors of fa_flex_forward, FA_ERR_UNSUPPORTED
+ * (other block sizes), FA_ERR_INVALID_ARG (chunk_blocks < 1, workspace NULL or misaligned),
+ * FA_ERR_BUFFER_TOO_SMALL. */
+FA_API size_t fa_forward_split_workspace_bytes(const fa_block_mask* block_mask, int32_t B, int32_t Hq, int32_t d,
+                                               int32_t chunk_blocks);
+FA_API fa_status fa_flex_forward_split(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
+                                       const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype,
+                                       float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN,
+                                       int32_t d, int32_t chunk_blocks, void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_status, fa_stream_t stream);
+
 /* Same as fa_flex_forward but always uses the mma.sync kernel (a second, independent kernel over the
  * same tables; used to cross-check the tcgen05 path). */
 FA_API fa_status fa_flex_forward_mma(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
