@@ -196,6 +196,16 @@ def max_over_ranks(ms: float, dist=None, device=None) -> float:
     return float(t.item())
 
 
+def sum_over_ranks(x: float, dist=None, device=None) -> float:
+    """The job's work: all-reduce SUM of each rank's own work (every unit belongs to one rank)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
 def job_tflops(world: int, flop_per_rank: float, ms_step: float) -> float:
     """Whole-job throughput: every rank processes its own shard of flop_per_rank per step (weak scaling)."""
     return world * flop_per_rank / (ms_step * 1e-3) / 1e12
@@ -248,13 +258,13 @@ class Prefill:
     """One prefill workload resident on the device: inputs, rule, BlockMask, outputs (fp32 O, as the
     tolerance needs), and the work counts of its visited blocks."""
 
-    def __init__(self, name, dev):
+    def __init__(self, name, dev, w=None):
         import numpy as np
         import torch
 
         from block_sparse_masked_create_gb300 import fa, workloads
         self.name = name
-        w = self.w = make_workload(name).generate()
+        w = self.w = make_workload(name).generate() if w is None else w
         self.q = workloads.bf16_torch(w.q_bits, dev)
         self.k = workloads.bf16_torch(w.k_bits, dev)
         self.v = workloads.bf16_torch(w.v_bits, dev)
@@ -303,6 +313,47 @@ class Prefill:
     def config(self):
         w = self.w
         return f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} N={w.q_len} d={w.d} Bq=Bk={w.bq}"
+
+
+class Shard:
+    """One rank's share of a workload partitioned by (batch row, KV head) units: its pieces (each a local
+    problem with its own mask), run one after the other; the same interface as Prefill."""
+
+    def __init__(self, name, parts, desc):
+        self.name, self.parts, self.desc = name, parts, desc
+        self.w = parts[0].w
+        self.phys_flops = sum(p.phys_flops for p in parts)
+        self.visited = sum(p.visited for p in parts)
+        lp = [p.logical_pairs for p in parts]
+        self.logical_pairs = None if any(x is None for x in lp) else sum(lp)
+        self.stats = [sum(p.stats[i] for p in parts) for i in range(3)] + [max(p.stats[3] for p in parts)]
+        self.launches = sum(p.launches for p in parts)
+        self.status = parts[0].status
+
+    def mask(self):
+        for p in self.parts:
+            p.mask()
+
+    def forward(self):
+        for p in self.parts:
+            p.forward()
+
+    def step(self):
+        self.mask()
+        self.forward()
+
+    def row_lengths(self):
+        import numpy as np
+        ln = []
+        for p in self.parts:
+            t = p.bm.tables()
+            ln.append((t["kv_num"] + t["full_kv_num"]).flatten().cpu().numpy().astype(np.float64))
+        ln = np.concatenate(ln)
+        return {"mean": float(ln.mean()), "p50": float(np.percentile(ln, 50)), "p95": float(np.percentile(ln, 95)),
+                "max": int(ln.max()), "rows": int(ln.size), "nk": int(self.parts[0].bm.c.nk)}
+
+    def config(self):
+        return self.desc
 
 
 def timed_steps(pf, steps, stream):
@@ -427,9 +478,21 @@ def ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     pk = peaks()
-    pf = Prefill(args.workload, dev)
-    w, q, k, v, out, lse, status, bm, sc = pf.w, pf.q, pf.k, pf.v, pf.out, pf.lse, pf.status, pf.bm, pf.sc
+    if world > 1:
+        # the workload with its batch scaled by the number of ranks, partitioned by (batch row, KV head)
+        # units: each rank builds masks for and runs only its own units (weak scaling, no collective)
+        from block_sparse_masked_create_gb300 import partition
+        wg = make_workload(args.workload)
+        wg.B *= world
+        pieces = partition.pieces_for_rank(wg.B, wg.Hkv, world, rank)
+        parts = [Prefill(args.workload, dev, w=partition.slice_prefill(wg, pc)[0]) for pc in pieces]
+        pf = Shard(args.workload, parts, pf_config(wg) + f", rank {rank} of {world}: (b, h_kv) pieces {pieces}")
+    else:
+        pf = Prefill(args.workload, dev)
+        parts = [pf]
+    w, status = pf.w, pf.status
     phys_flops = pf.phys_flops
+    step_launches = pf.launches  # per piece: [document runs,] classify, transpose, forward
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
@@ -459,26 +522,32 @@ def ours(args, rank, world, local_rank):
     if dist:
         dist.barrier()
     ms = max_over_ranks(ms, dist, dev)
+    total_flops = sum_over_ranks(phys_flops, dist, dev)   # every unit counted once, on the rank that owns it
     st_code = fa.check_status(status)
     ms_step = ms / args.steps
-    value = job_tflops(world, phys_flops, ms_step)
+    value = total_flops / (ms_step * 1e-3) / 1e12
     summ = prefill_summary(pf, pk, fwd_ms, mask_ms, ms_step, world)
 
     # ---------------- end to end through the public API with host buffers
     e2e = None
     if rank == 0 or world > 1:
-        hq = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True).copy_(q)
-        hk = torch.empty(k.shape, dtype=torch.bfloat16, pin_memory=True).copy_(k)
-        hv = torch.empty(v.shape, dtype=torch.bfloat16, pin_memory=True).copy_(v)
-        ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        hl = torch.empty(lse.shape, dtype=torch.float32, pin_memory=True)
-
-        hws = torch.empty(fa.forward_host_workspace_bytes(w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, out.dtype),
-                          dtype=torch.uint8, device=dev)
+        hosts = []
+        for p in parts:
+            hq = torch.empty(p.q.shape, dtype=torch.bfloat16, pin_memory=True).copy_(p.q)
+            hk = torch.empty(p.k.shape, dtype=torch.bfloat16, pin_memory=True).copy_(p.k)
+            hv = torch.empty(p.v.shape, dtype=torch.bfloat16, pin_memory=True).copy_(p.v)
+            ho = torch.empty(p.out.shape, dtype=p.out.dtype, pin_memory=True)
+            hl = torch.empty(p.lse.shape, dtype=torch.float32, pin_memory=True)
+            pw = p.w
+            hws = torch.empty(fa.forward_host_workspace_bytes(pw.B, pw.Hq, pw.Hkv, pw.q_len, pw.kv_len, pw.d,
+                                                              p.out.dtype), dtype=torch.uint8, device=dev)
+            hosts.append((p, hq, hk, hv, ho, hl, hws))
 
         def e2e_step():  # host tensors in and out: fa_flex_forward_host streams them through the GPU
-            pf.mask()
-            fa.flex_forward_host(hq, hk, hv, bm, sc, w.scale, out=ho, lse=hl, workspace=hws, status=status)
+            for (p, hq, hk, hv, ho, hl, hws) in hosts:
+                p.mask()
+                fa.flex_forward_host(hq, hk, hv, p.bm, p.sc, p.w.scale, out=ho, lse=hl, workspace=hws,
+                                     status=p.status)
 
         for _ in range(max(3, args.warmup // 2)):
             e2e_step()
@@ -490,15 +559,24 @@ def ours(args, rank, world, local_rank):
             e2e_step()
         e2.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = s2.elapsed_time(e2) / n2
-        bi = 3 * q.numel() * 2
-        bo = out.numel() * out.element_size() + lse.numel() * 4
-        ceil = copy_ceiling(hq, hk, hv, ho, hl, q, k, v, out, lse, dev)
-        e2e = {"value": world * phys_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e_ms = max_over_ranks(s2.elapsed_time(e2) / n2, dist, dev)
+        bi = sum(3 * p.q.numel() * 2 for p in parts)
+        bo = sum(p.out.numel() * p.out.element_size() + p.lse.numel() * 4 for p in parts)
+        e2e = {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
-               "api": "fa_flex_forward_host (pinned host Q, K, V, O, LSE)",
-               "copy_ceiling": ceil, "copy_floor_over_e2e": ceil["duplex_ms"] / e2e_ms}
-        del hq, hk, hv, ho, hl, hws
+               "api": "fa_flex_forward_host (pinned host Q, K, V, O, LSE)"}
+        if world == 1:
+            (_, hq, hk, hv, ho, hl, _) = hosts[0]
+            ceil = copy_ceiling(hq, hk, hv, ho, hl, pf.q, pf.k, pf.v, pf.out, pf.lse, dev)
+            e2e.update({"copy_ceiling": ceil, "copy_floor_over_e2e": ceil["duplex_ms"] / e2e_ms})
+        del hosts
+
+    # the measurements below are of one GPU: they run with a single rank only
+    if world > 1:
+        args.no_backward = args.no_paged = args.no_others = args.no_split = args.no_decode = True
+        args.no_cpu = True
+    else:
+        w, q, k, v, out, lse, bm, sc = pf.w, pf.q, pf.k, pf.v, pf.out, pf.lse, pf.bm, pf.sc
 
     # ---------------- backward over the same mask and forward outputs (secondary line item)
     bwd_line = None
@@ -517,7 +595,7 @@ def ours(args, rank, world, local_rank):
     # ---------------- the other prefill workloads, each timed like the main one
     others = {}
     if not args.no_others:
-        del pf, q, k, v, out, lse
+        del pf, parts, q, k, v, out, lse
         torch.cuda.empty_cache()
         for name in ("cfg2", "cfg3", "cfg4"):
             if name != args.workload:
@@ -555,14 +633,16 @@ def ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": pf_config(w), "step": "fa_create_block_mask + fa_flex_forward", "out": "fp32 O, fp32 LSE",
+        "config": {"workload": pf_config(w) if world == 1 else summ["workload"],
+                   "step": "fa_create_block_mask + fa_flex_forward", "out": "fp32 O, fp32 LSE",
                    "l2": "inputs larger than the 129 MB L2 (no flush)",
-                   "parallelism": f"replica x{world} (independent (b,h) shards, no collective)"},
+                   "parallelism": "1 GPU" if world == 1 else
+                   f"{world} ranks, batch x{world}, partitioned by (batch row, KV head) units, no collective"},
     }
     line.update({k_: v_ for k_, v_ in summ.items() if k_ != "workload"})
     line.update({
         "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": args.steps * (3 + (1 if w.doc_ids is not None else 0)),
+        "gpu_launches": args.steps * step_launches,
         "clocks": clk.summary(), "status": fa.status_string(st_code), "wall_s": wall,
     })
     if others:
