@@ -499,7 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sl2 = a.scale * kLog2e;
       float slope2 = 0.f;
       if (SK == SK_ALIBI || SK == SK_GENERIC) slope2 = a.score.alibi ? __ldg(a.score.alibi + TT.h) * kLog2e : 0.f;
-      const float mult = SK == SK_NONE ? sl2 : 1.f;  // SK_NONE defers the scale into the exponent's FMA
+      // the factor the exponent's FMA applies: the scale (no score rule) or log2(e) c (soft-cap), else 1
+      const float mult = SK == SK_NONE ? sl2 : SK == SK_SOFTCAP ? a.score.softcap * kLog2e : 1.f;
       float m_ref = -INFINITY;  // reference max (log2 domain) used for P and for O
       // the row sum of P (for the LSE), and the correction that turns it into the sum O is divided by: per
       // block, the bf16 rounding error of the row's largest P (see the P loop)
@@ -544,14 +545,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             f2_unpack(f2_fma(f2_pack(x[i], x[i + 1]), s2, bias), x[i], x[i + 1]);
           }
         } else if (SK == SK_SOFTCAP) {
-          // log2(e) c tanh(scale x / c), packed multiplies around the tanh
-          const float ain = a.scale * a.score.inv_softcap, aout = a.score.softcap * kLog2e;
-          const uint64_t in2 = f2_pack(ain, ain), out2 = f2_pack(aout, aout);
+          // tanh(scale x / c); the factor log2(e) c is applied in the exponent's FMA (mult)
+          const float ain = a.scale * a.score.inv_softcap;
+          const uint64_t in2 = f2_pack(ain, ain);
 #pragma unroll
           for (int i = 0; i < 128; i += 2) {
             float u0, u1;
             f2_unpack(f2_mul(f2_pack(x[i], x[i + 1]), in2), u0, u1);
-            f2_unpack(f2_mul(f2_pack(tanh_approx(u0), tanh_approx(u1)), out2), x[i], x[i + 1]);
+            x[i] = tanh_approx(u0);
+            x[i + 1] = tanh_approx(u1);
           }
         } else if (SK == SK_GENERIC) {
           for (int i = 0; i < 128; ++i) {
