@@ -16,33 +16,46 @@
 namespace fa {
 namespace {
 
-__global__ void __launch_bounds__(128) mask_split_kernel(MaskOut S, int C, int ncm, MaskOut D) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+// One warp per (query block row, chunk). The row's visited blocks in column order are the merge of its
+// full and partial lists (each ascending, no column in both); the number of full blocks among the first
+// k of them is found by a binary search over the two lists (a merge path), so every lane places its own
+// positions of the chunk without walking the row.
+__device__ __forceinline__ int full_before(const int32_t* fi, int nf, const int32_t* pi, int np, int k) {
+  int lo = max(0, k - np), hi = min(k, nf);
+  while (lo < hi) {  // more full blocks while the next full one precedes the partial one it would displace
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(fi + mid) < __ldg(pi + (k - mid - 1))) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(256) mask_split_kernel(MaskOut S, int C, int ncm, MaskOut D) {
+  const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int bh = blockIdx.y;  // b_m * Hm + h_m
-  if (r >= S.nq) return;
+  if (w >= S.nq * ncm) return;
+  const int r = w / ncm, c = w - r * ncm;
   const size_t srow = (size_t)bh * S.nq + r;
   const int nf = S.full_kv_num[srow], np = S.kv_num[srow];
   const int32_t* fi = S.full_kv_idx + srow * S.nk;
   const int32_t* pi = S.kv_idx + srow * S.nk;
+  const int n = nf + np;
+  const int k0 = min(c * C, n), k1 = min(k0 + C, n);  // the chunk's positions in column order
+  const int f0 = full_before(fi, nf, pi, np, k0), p0 = k0 - f0;
+  const int cf = full_before(fi, nf, pi, np, k1) - f0, cp = (k1 - k0) - cf;
   const size_t nqd = (size_t)S.nq * ncm;
-  int f = 0, p = 0;
-  for (int c = 0; c < ncm; ++c) {
-    const size_t drow = (size_t)bh * nqd + (size_t)r * ncm + c;
-    int32_t* dfi = D.full_kv_idx + drow * C;
-    int32_t* dpi = D.kv_idx + drow * C;
-    int cf = 0, cp = 0;
-    for (int k = 0; k < C && (f < nf || p < np); ++k) {  // the next C blocks in column order
-      const int colf = f < nf ? fi[f] : 0x7FFFFFFF, colp = p < np ? pi[p] : 0x7FFFFFFF;
-      if (colp < colf) {
-        dpi[cp++] = colp;
-        ++p;
-      } else {
-        dfi[cf++] = colf;
-        ++f;
-      }
-    }
-    for (int k = cf; k < C; ++k) dfi[k] = 0;  // unused slots 0, as in every table
-    for (int k = cp; k < C; ++k) dpi[k] = 0;
+  const size_t drow = (size_t)bh * nqd + (size_t)r * ncm + c;
+  int32_t* dfi = D.full_kv_idx + drow * C;
+  int32_t* dpi = D.kv_idx + drow * C;
+  for (int k = k0 + lane; k < k1; k += 32) {
+    const int f = full_before(fi, nf, pi, np, k);
+    const int vf = f < nf ? __ldg(fi + f) : 0x7FFFFFFF, vp = k - f < np ? __ldg(pi + (k - f)) : 0x7FFFFFFF;
+    if (vf < vp) dfi[f - f0] = vf;
+    else dpi[(k - f) - p0] = vp;
+  }
+  for (int k = cf + lane; k < C; k += 32) dfi[k] = 0;  // unused slots 0, as in every table
+  for (int k = cp + lane; k < C; k += 32) dpi[k] = 0;
+  if (lane == 0) {
     D.full_kv_num[drow] = cf;
     D.kv_num[drow] = cp;
     D.row_order[(size_t)bh * nqd + (size_t)c * S.nq + (S.nq - 1 - r)] = r * ncm + c;
@@ -102,8 +115,8 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const float* __restr
 }  // namespace
 
 cudaError_t launch_mask_split(const MaskOut& S, int C, int ncm, const MaskOut& D, cudaStream_t st) {
-  dim3 grid((S.nq + 127) / 128, S.Bm * S.Hm);
-  mask_split_kernel<<<grid, 128, 0, st>>>(S, C, ncm, D);
+  dim3 grid((unsigned)(((int64_t)S.nq * ncm + 7) / 8), S.Bm * S.Hm);
+  mask_split_kernel<<<grid, 256, 0, st>>>(S, C, ncm, D);
   return cudaGetLastError();
 }
 
