@@ -55,6 +55,7 @@ struct Tc5Cfg {
   static constexpr int kOffBar = kOffRing + kStages * kSlotBytes;  // mbarriers, TMEM address, abort flag
   static constexpr int kSmem = kOffBar + 512;
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert((11 + 2 * kStages) * 8 + 16 <= 512, "barrier region");
   static constexpr uint32_t kTmemCols = 512;
   // tensor-memory columns: S_t at [256 t, 256 t + 128), with P_t (bf16 pairs: keys 2i, 2i+1 in column i)
   // over its first 64 columns; O_t at [256 t + 128, 256 t + 128 + D)
@@ -215,8 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* const bar_full = bars + 8;   // [NST] ring slot landed
   uint64_t* const bar_empty = bars + 8 + NST;  // [NST] ring slot consumed
   uint64_t& bar_drain = bars[8 + 2 * NST];
-  uint32_t& s_tmem = *reinterpret_cast<uint32_t*>(bars + 9 + 2 * NST);
-  int32_t& s_abort = *(reinterpret_cast<int32_t*>(bars + 9 + 2 * NST) + 1);
+  uint64_t& bar_info = bars[9 + 2 * NST];  // the union summary below is written
+  uint32_t& s_tmem = *reinterpret_cast<uint32_t*>(bars + 10 + 2 * NST);
+  int32_t& s_abort = *(reinterpret_cast<int32_t*>(bars + 10 + 2 * NST) + 1);
+  // union summary from the MMA warp: elements, each tile's last element (-1: none), tile 1 visits tile 0's last
+  volatile int32_t* const s_info = reinterpret_cast<volatile int32_t*>(bars + 11 + 2 * NST);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (smem_u32(smem) & 1023u) {  // uniform across the CTA, before any barrier or allocation
@@ -233,7 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Tile T1 = make_tile(a, b, h1, r1);
   // both tiles read the same K / V (one batch row, one KV head): each block of the union of their lists is
   // loaded once; the two lists are the same when they come from the same mask row
-  const bool same_list = T1.valid && T1.n > 0 && T0.n > 0 && T0.full_idx == T1.full_idx && T0.part_idx == T1.part_idx;
 
   uint8_t* sQ0 = smem;
   uint8_t* sQ1 = smem + C::kQBytes;
@@ -279,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_empty[s], 1);
       }
       mbar_init(&bar_drain, 1);
+      mbar_init(&bar_info, 1);
       fence_mbar_init();
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
@@ -427,9 +431,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     Union mw;
     mw.init(T0, T1, desc);
     int np[2] = {0, 0};  // P blocks consumed so far per tile
+    int uk = 0, last0 = -1, last1 = -1, both0 = 0;  // union elements taken; each tile's last; tile 1 on last0
+    bool info = false;
     while (ok) {
       cur.live = !mw.done();
-      if (cur.live) mw.take(T0, T1, desc, cur.in0, cur.in1);
+      if (cur.live) {
+        mw.take(T0, T1, desc, cur.in0, cur.in1);
+        if (cur.in0) {
+          last0 = uk;
+          both0 = cur.in1;
+        }
+        if (cur.in1) last1 = uk;
+        ++uk;
+      } else if (!info) {  // the union is known: its summary for the epilogues' staging plans
+        if (lane == 0) {
+          s_info[0] = uk;
+          s_info[1] = last0;
+          s_info[2] = last1;
+          s_info[3] = both0;
+          mbar_arrive(&bar_info);
+        }
+        __syncwarp();
+        info = true;
+      }
       if (!cur.live && !prev.live) break;
       // slots of V(prev) and K(cur), taken before the waits for P, so that their barrier waits are off the
       // path from P to the next products
@@ -464,11 +488,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2;
     const int row = (warp & 3) * 32 + lane;
     const Tile TT = t ? T1 : T0;
-    // the epilogue's staging plan, fixed here so that nothing of the other tile stays live in the loop
-    const int n_loads = 2 * (same_list ? T0.n : T0.n + T1.n);  // loads issued: K and V per union element
-    const bool single = !(T0.n > 0 && T1.valid && T1.n > 0);
-    const bool ring_stage = a.out_f32 && (single || same_list);
-    const int slot_base = single ? 1 : (t ? 4 : 2);
     uint8_t* const sQt = t ? sQ1 : sQ0;
     const int q_row = TT.rq * 128 + row;  // query position within the sequence (rule, score, validity)
     const int o_row = TT.r * 128 + row;   // output row (the same unless rows are split)
@@ -650,18 +669,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool empty = m_ref == -INFINITY;
       const float inv = empty ? 0.f : 1.f / (le + lc);
       if (ok && q_row < a.q_len) Lg[o_row] = empty ? -INFINITY : (m_ref + __log2f(le)) * kLn2;
-      // fp32 O ([128][D], D / 32 boxes of [128][32]: 128-byte rows, 128-byte swizzle) is staged in K / V
-      // ring slots that no product reads any more and no load refills: with a single tile in use, its last
-      // product is the CTA's last MMA and every slot is free then (it takes the slots of the last two
-      // loads); with two tiles on the same mask row, every load but the last (V of the last element, still
-      // read by tile 1's last product) has been consumed once tile 0's last product completed, so tile 0
-      // takes the slots of the loads 2 and 3 from the end and tile 1 those of the loads 4 and 5 (five
-      // consecutive loads sit in distinct slots). Otherwise O goes through the tile's Q buffer (free: every
-      // product reading it has completed): bf16 in one round ([128][64] boxes), fp32 in rounds of
-      // QB = D / 64 boxes.
+      // fp32 O ([128][D], D / 32 boxes of [128][32]: 128-byte rows, 128-byte swizzle; two ring slots) is
+      // staged in K / V ring slots that no product reads any more and no load refills, in one round. Loads
+      // are numbered K(u0) = 0, V(u0) = 1, K(u1) = 2, ... over the union's U elements (n = 2 U loads); load i
+      // sits in slot i % NST and has not been refilled if i >= n - NST. The tile whose last product comes
+      // first (earlier last element, or the same one and tile 0) finds free every such load up to the V of
+      // its last element (which tile 1 may still read when tile 0 is first) and takes the two lowest; the
+      // other tile's last product is the CTA's last, so it takes the two highest the first did not take.
+      // Without two free slots, O goes through the tile's Q buffer (free: every product reading it has
+      // completed): bf16 in one round ([128][64] boxes), fp32 in rounds of QB = D / 64 boxes.
+      int stg0 = -1, stg1 = -1;  // ring slots of the fp32 O, or -1: the Q buffer
+      if (a.out_f32 && ok) {
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_info, 0u, wc));
+        if (ok) {
+          const int n = 2 * s_info[0], lo = max(0, n - NST);
+          const int l[2] = {s_info[1], s_info[2]};
+          const int o = 1 - t;
+          const bool first = l[o] >= 0 && (l[t] < l[o] || (l[t] == l[o] && t == 0));
+          // the first tile's free range ends at its last V, or one before it when tile 1 reads that V too
+          const int f = first ? t : o;
+          const int hi_f = l[o] < 0 ? -1 : 2 * l[f] + 1 - (f == 0 && s_info[3] ? 1 : 0);
+          const bool f_ring = l[o] >= 0 && hi_f - lo + 1 >= 2;
+          if (first) {
+            if (f_ring) {
+              stg0 = lo;
+              stg1 = lo + 1;
+            }
+          } else {  // the CTA's last product is this tile's: every load n - NST .. n - 1 is free
+            int k = n - 1;
+            if (f_ring && k <= lo + 1) k = -1;
+            if (k >= lo) {
+              stg0 = k;
+              stg1 = k - 1;
+              if (f_ring && stg1 <= lo + 1) stg0 = stg1 = -1;
+            }
+          }
+          if (stg1 < lo) stg0 = stg1 = -1;
+        }
+      }
+      const bool ring_stage = stg0 >= 0;
       auto box_ring = [&](int kb) -> uint8_t* {
-        int sl = (n_loads - (slot_base + (kb * 16384) / C::kSlotBytes)) % NST;
-        sl = sl < 0 ? sl + NST : sl;
+        const int sl = ((kb * 16384) / C::kSlotBytes ? stg1 : stg0) % NST;
         return sRing + sl * C::kSlotBytes + (kb * 16384) % C::kSlotBytes;
       };
       constexpr int QB = D / 64;
