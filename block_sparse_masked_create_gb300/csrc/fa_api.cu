@@ -219,8 +219,11 @@ int encode_tmap_f32(CUtensorMap* m, const void* base, int rank, const uint64_t* 
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Decode splits of 4096 tokens: long enough that a CTA's start-up (barriers, page-table reads, the first
+// copies in flight) is small against its 2 MiB of K/V at d = 128, short enough that the 64-request paged
+// decode still runs about 14 waves of CTAs (89.8 % of the measured HBM copy rate against 86.9 % with 2048)
 static int decode_pages_per_split(int page, int max_pages) {
-  int ps = std::max(1, 2048 / std::max(page, 1));
+  int ps = std::max(1, 4096 / std::max(page, 1));
   return std::min(ps, std::max(max_pages, 1));
 }
 

@@ -337,7 +337,7 @@ FA_API fa_status fa_flex_decode(const void* q, const void* k_pages, const void* 
  *    FA_ERR_BUFFER_TOO_SMALL and launches nothing (fa_decode_noalloc_scratch_bytes() reports the size).
  *    Every other argument is checked first, with the codes fa_flex_decode returns for it. The need is
  *    about Bz * Hq * n_splits * (d + 3) * 4 bytes, n_splits = ceil(max_pages / min(max_pages,
- *    2048 / page)): with d = 128, 128-token pages, a 32768-token table (16 splits) and Hq = 32, up to 125
+ *    4096 / page)): with d = 128, 128-token pages, a 32768-token table (8 splits) and Hq = 32, up to 250
  *    requests fit.
  *  - Sharing: all calls use the same array. Calls that overlap on the GPU (different streams with no
  *    ordering between them) race on it; calls on one stream are fine. Nothing in it needs clearing
