@@ -582,8 +582,15 @@ fa_status fa_flex_forward_paged(const void* q, const void* k_pages, const void* 
 // copies in, the kernels (two streams, so a chunk's CTAs can fill the SMs the previous chunk's short CTAs
 // free) and the copies out run on separate streams, so each chunk's copies overlap its neighbours' work.
 // ------------------------------------------------------------------------------------------------
+// The host path streams about kHostChunks chunks (whole KV heads of one batch row each) through
+// kHostSlots device buffers: a chunk's copies in wait only for the copies out of the chunk kHostSlots
+// earlier. Measured on cfg2 (201 MB in, 135 MB out, 1.14 ms for the copies alone in both directions): 3
+// slots x 8 chunks 1.40 ms, 2 x 8 1.47 ms, 4 x 8 and 3 x 4 1.40 ms, 3 x 16 1.46 ms, 3 x 32 1.77 ms (smaller
+// copies run below the link's rate).
+constexpr int kHostSlots = 3;
+constexpr int kHostChunks = 8;
 struct HostPlan {
-  int ck, g, n_chunks, chunks_per_b;
+  int ck, g, n_chunks, chunks_per_b, n_slots;
   size_t q_bytes, kv_bytes, o_bytes, l_bytes, slot_bytes;
 };
 
@@ -592,11 +599,11 @@ static int host_plan(int B, int Hq, int Hkv, int Q_LEN, int KV_LEN, int d, int o
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (out_dtype != FA_OUT_BF16 && out_dtype != FA_OUT_F32) return FA_ERR_INVALID_ARG;
   P->g = Hq / Hkv;
-  // about eight chunks per call (enough to overlap), never more than one batch row per chunk
   const int units = B * Hkv;
-  P->ck = std::max(1, std::min(Hkv, units / 8));
+  P->ck = std::max(1, std::min(Hkv, units / kHostChunks));
   P->chunks_per_b = (Hkv + P->ck - 1) / P->ck;
   P->n_chunks = B * P->chunks_per_b;
+  P->n_slots = std::min(kHostSlots, P->n_chunks);
   const size_t qh = (size_t)Q_LEN * d, kh = (size_t)KV_LEN * d;
   P->q_bytes = align256((size_t)P->ck * P->g * qh * 2);
   P->kv_bytes = align256((size_t)P->ck * kh * 2);
@@ -609,7 +616,7 @@ static int host_plan(int B, int Hq, int Hkv, int Q_LEN, int KV_LEN, int d, int o
 size_t fa_forward_host_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN, int32_t d,
                                        int32_t out_dtype) {
   HostPlan P;
-  return host_plan(B, Hq, Hkv, Q_LEN, KV_LEN, d, out_dtype, &P) == FA_OK ? 2 * P.slot_bytes : 0;
+  return host_plan(B, Hq, Hkv, Q_LEN, KV_LEN, d, out_dtype, &P) == FA_OK ? P.n_slots * P.slot_bytes : 0;
 }
 
 fa_status fa_flex_forward_host(const void* host_q, const void* host_k, const void* host_v,
@@ -622,20 +629,19 @@ fa_status fa_flex_forward_host(const void* host_q, const void* host_k, const voi
   HostPlan P;
   int s = host_plan(B, Hq, Hkv, Q_LEN, KV_LEN, d, out_dtype, &P);
   if (s != FA_OK) return (fa_status)s;
-  if (workspace_bytes < 2 * P.slot_bytes) return FA_ERR_BUFFER_TOO_SMALL;
+  if (workspace_bytes < P.n_slots * P.slot_bytes) return FA_ERR_BUFFER_TOO_SMALL;
   if (reinterpret_cast<uintptr_t>(dev_workspace) & 255u) return FA_ERR_INVALID_ARG;
   const fa_block_mask& M = *block_mask;
   if (M.q_len != Q_LEN || M.kv_len != KV_LEN || !(M.Bm == 1 || M.Bm == B) || !(M.Hm == 1 || M.Hm == Hq))
     return FA_ERR_SHAPE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaStream_t s_in = nullptr, s_out = nullptr, s_c1 = nullptr;
-  cudaEvent_t ev_start = nullptr, ev_in[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr},
-              ev_free[2] = {nullptr, nullptr};
+  cudaEvent_t ev_start = nullptr, ev_in[kHostSlots] = {}, ev_done[kHostSlots] = {}, ev_free[kHostSlots] = {};
   bool cuda_ok = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) == cudaSuccess &&
                  cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) == cudaSuccess &&
                  cudaStreamCreateWithFlags(&s_c1, cudaStreamNonBlocking) == cudaSuccess &&
                  cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) == cudaSuccess;
-  for (int i = 0; i < 2 && cuda_ok; ++i)
+  for (int i = 0; i < P.n_slots && cuda_ok; ++i)
     cuda_ok = cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&ev_done[i], cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&ev_free[i], cudaEventDisableTiming) == cudaSuccess;
@@ -647,8 +653,8 @@ fa_status fa_flex_forward_host(const void* host_q, const void* host_k, const voi
   const size_t oel = out_dtype == FA_OUT_F32 ? 4 : 2;
   int status = cuda_ok ? FA_OK : FA_ERR_CUDA;
   for (int c = 0; c < P.n_chunks && status == FA_OK; ++c) {
-    const int slot = c & 1;
-    cudaStream_t sc = slot ? s_c1 : st;  // this slot's kernels
+    const int slot = c % P.n_slots;
+    cudaStream_t sc = (c & 1) ? s_c1 : st;  // the chunk's kernels (two streams, so that they may overlap)
     const int b = c / P.chunks_per_b, hk0 = (c % P.chunks_per_b) * P.ck;
     const int nk = std::min(P.ck, Hkv - hk0), h0 = hk0 * P.g, nq = nk * P.g;
     uint8_t* base = static_cast<uint8_t*>(dev_workspace) + slot * P.slot_bytes;
@@ -658,7 +664,7 @@ fa_status fa_flex_forward_host(const void* host_q, const void* host_k, const voi
     void* dout = base + P.q_bytes + 2 * P.kv_bytes;
     float* dlse = reinterpret_cast<float*>(base + P.q_bytes + 2 * P.kv_bytes + P.o_bytes);
     // copies in, once the copies out of the chunk that used this slot before have finished
-    if (c >= 2 && cudaStreamWaitEvent(s_in, ev_free[slot], 0) != cudaSuccess) { status = FA_ERR_CUDA; break; }
+    if (c >= P.n_slots && cudaStreamWaitEvent(s_in, ev_free[slot], 0) != cudaSuccess) { status = FA_ERR_CUDA; break; }
     const size_t qoff = ((size_t)b * Hq + h0) * qh, koff = ((size_t)b * Hkv + hk0) * kh;
     if (cudaMemcpyAsync(dq, static_cast<const uint8_t*>(host_q) + qoff * 2, (size_t)nq * qh * 2,
                         cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
@@ -716,7 +722,7 @@ fa_status fa_flex_forward_host(const void* host_q, const void* host_k, const voi
   // `stream` completes after the last copy out; the side streams and events are released when idle
   if (s_out && cudaEventRecord(ev_start, s_out) == cudaSuccess) cudaStreamWaitEvent(st, ev_start, 0);
   if (s_c1 && ev_in[0] && cudaEventRecord(ev_in[0], s_c1) == cudaSuccess) cudaStreamWaitEvent(st, ev_in[0], 0);
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < kHostSlots; ++i) {
     if (ev_in[i]) cudaEventDestroy(ev_in[i]);
     if (ev_done[i]) cudaEventDestroy(ev_done[i]);
     if (ev_free[i]) cudaEventDestroy(ev_free[i]);

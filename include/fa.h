@@ -209,7 +209,7 @@ FA_API fa_status fa_flex_forward(const void* q, const void* k, const void* v, co
 
 /* The same forward with Q, K, V, O and LSE in host memory (pinned memory for full copy speed), for callers
  * whose tensors live on the host: the batch's KV heads are cut into chunks (about eight per call) that
- * stream through two device slots of `dev_workspace`; each chunk's copies in, its kernel and its copies
+ * stream through three device slots of `dev_workspace`; each chunk's copies in, its kernel and its copies
  * out run on separate streams, so copies overlap the neighbouring chunks' work. The mask stays on the
  * device (build it with fa_create_block_mask on `stream` first).
  *   host_q, host_k, host_v, host_out, host_lse  host pointers, layouts as fa_flex_forward; they must stay
