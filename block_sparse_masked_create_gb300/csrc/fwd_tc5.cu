@@ -512,11 +512,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t off_b = a.rule.q_offset ? (int64_t)__ldg(a.rule.q_offset + (M.Bm > 1 ? b : 0)) : 0;
       const int64_t ig = (int64_t)q_row + off_b;
       const int bm = M.Bm > 1 ? b : 0;
-      const int doc_i = a.rule.any_doc ? doc_at(a.rule, bm, ig) : -1;
-      // document equality as the column interval of this row's run when the ids never decrease
-      const bool runs = a.rule.any_doc && ig >= 0 && ig < a.rule.doc_len && doc_runs_usable(a.rule, bm);
-      int64_t run_lo = 0, run_hi = 0;
-      if (runs) doc_run_of(a.rule, bm, ig, run_lo, run_hi);
       const float sl2 = a.scale * kLog2e;
       float slope2 = 0.f;
       if (SK == SK_ALIBI || SK == SK_GENERIC) slope2 = a.score.alibi ? __ldg(a.score.alibi + TT.h) * kLog2e : 0.f;
@@ -543,6 +538,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int w = (int)max((int64_t)0, min((int64_t)128, (int64_t)a.kv_len - j0));
           bits = {{0u, 0u, 0u, 0u}};
           if (q_row < a.q_len && w > 0) {
+            // the row's document and (ids that never decrease) its run as a column interval, looked up per
+            // partial block so that they hold no registers through the block loop
+            const int doc_i = a.rule.any_doc ? doc_at(a.rule, bm, ig) : -1;
+            const bool runs = a.rule.any_doc && ig >= 0 && ig < a.rule.doc_len && doc_runs_usable(a.rule, bm);
+            int64_t run_lo = 0, run_hi = 0;
+            if (runs) doc_run_of(a.rule, bm, ig, run_lo, run_hi);
             bits = rule_row_bits(a.rule, ig, j0, w, doc_i, [&](int dq) {
               if (runs) return range_bits(clamp_rel(run_lo - j0, w), clamp_rel(run_hi - j0, w));
               return doc_bits<4>(w, dq, [&](int cc) { return doc_at(a.rule, bm, j0 + cc); });
