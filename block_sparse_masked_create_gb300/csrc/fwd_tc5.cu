@@ -55,7 +55,7 @@ struct Tc5Cfg {
   static constexpr int kOffBar = kOffRing + kStages * kSlotBytes;  // mbarriers, TMEM address, abort flag
   static constexpr int kSmem = kOffBar + 512;
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
-  static_assert((11 + 2 * kStages) * 8 + 16 <= 512, "barrier region");
+  static_assert((13 + 2 * kStages) * 8 + 4 * kStages <= 512, "barrier region");
   static constexpr uint32_t kTmemCols = 512;
   // tensor-memory columns: S_t at [256 t, 256 t + 128), with P_t (bf16 pairs: keys 2i, 2i+1 in column i)
   // over its first 64 columns; O_t at [256 t + 128, 256 t + 128 + D)
@@ -138,11 +138,46 @@ struct Walk {
 };
 __device__ __forceinline__ int key_col(int key, bool desc) { return desc ? -key : key; }
 
+// The same walk with the loaded column ids kept as loaded: the ordering keys are derived where they are
+// compared, so the load that advance() issues is first waited for at the next element rather than at once
+// (the producer walks the union between its loads; a cache round trip per element would delay them).
+struct LazyWalk {
+  int f, p, nf, np, vf, vp, dsc;
+  static __device__ __forceinline__ int load(const int32_t* idx, int n, int i, bool desc) {
+    const int k = i < n ? (desc ? n - 1 - i : i) : 0;
+    int v;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(idx + k));
+    return v;
+  }
+  __device__ __forceinline__ void init(const Tile& T, bool desc) {
+    f = p = 0;
+    nf = T.n_full;
+    np = T.n_part;
+    dsc = desc;
+    vf = load(T.full_idx, nf, 0, desc);
+    vp = load(T.part_idx, np, 0, desc);
+  }
+  __device__ __forceinline__ int kf() const { return f < nf ? (dsc ? -vf : vf) : INT_MAX; }
+  __device__ __forceinline__ int kp() const { return p < np ? (dsc ? -vp : vp) : INT_MAX; }
+  __device__ __forceinline__ int next_key() const { return min(kf(), kp()); }
+  __device__ __forceinline__ bool next_partial() const { return kp() < kf(); }
+  __device__ __forceinline__ void advance(const Tile& T, bool desc) {
+    if (kp() < kf()) {
+      ++p;
+      vp = load(T.part_idx, np, p, desc);
+    } else {
+      ++f;
+      vf = load(T.full_idx, nf, f, desc);
+    }
+  }
+};
+
 // The union of the two tiles' block sequences (both tiles read the same K / V: one batch row, one KV
-// head), in the same order; each element says which tiles visit it. The producer loads K and V of each
-// element once; the MMA warp issues each tile's products on its own elements.
+// head), in the same order; each element says which tiles visit it. The producer walks it, loads K and V of
+// each element once and passes the element's flags to the MMA warp with its K slot; the MMA warp issues each
+// tile's products on its own elements.
 struct Union {
-  Walk w0, w1;
+  LazyWalk w0, w1;
   __device__ __forceinline__ void init(const Tile& T0, const Tile& T1, bool desc) {
     w0.init(T0, desc);
     w1.init(T1, desc);
@@ -197,6 +232,51 @@ __device__ __forceinline__ void work_item(const FwdArgs& a, int pair_rows, int g
   }
 }
 
+// A whole product is issued from one asm statement: one elect.sync picks the issuing lane for all its
+// K-steps (an elect and a separate statement per K-step cost the single MMA warp more issue time than the
+// tensor core spends on the step). Operand offsets per K-step ks, in 16-byte descriptor units:
+//  S = Q K^T (K-major, 128-byte swizzle, [128][64] sub-tiles of 16 KiB): (ks / 4) * 1024 + (ks % 4) * 2 on
+//  both operands; the first step overwrites S, the others accumulate.
+//  O += P V: P (bf16 pairs) at tensor-memory column 8 ks, V rows 16 ks .. 16 ks + 15 at 128 ks; the first
+//  step accumulates only if `acc`.
+#define FA_MMA_HEAD                                                                                       \
+  "{\n\t.reg .pred P, Q, T;\n\t.reg .b64 da, db;\n\t.reg .b32 ta;\n\telect.sync _|P, 0xffffffff;\n\t" \
+  "setp.ne.b32 Q, %4, 0;\n\tsetp.eq.b32 T, %4, %4;\n\t"
+#define FA_QK_FIRST "@P tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, Q;\n\t"
+#define FA_QK_STEP(OFF) \
+  "add.s64 da, %1, " #OFF ";\n\tadd.s64 db, %2, " #OFF ";\n\t@P tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, T;\n\t"
+#define FA_PV_FIRST "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, Q;\n\t"
+#define FA_PV_STEP(COL, OFF)                                                                               \
+  "add.s32 ta, %1, " #COL ";\n\tadd.s64 db, %2, " #OFF ";\n\t@P tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, " \
+  "%3, T;\n\t"
+
+template <int NK>  // D / 16 K-steps
+__device__ __forceinline__ void mma_qk_product(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc, uint32_t idesc) {
+  static_assert(NK == 4 || NK == 8, "d = 64 or 128");
+  if constexpr (NK == 8) {
+    asm volatile(FA_MMA_HEAD FA_QK_FIRST FA_QK_STEP(2) FA_QK_STEP(4) FA_QK_STEP(6) FA_QK_STEP(1024) FA_QK_STEP(1026)
+                     FA_QK_STEP(1028) FA_QK_STEP(1030) "}" ::"r"(d_tmem),
+                 "l"(qdesc), "l"(kdesc), "r"(idesc), "r"(0u)
+                 : "memory");
+  } else {
+    asm volatile(FA_MMA_HEAD FA_QK_FIRST FA_QK_STEP(2) FA_QK_STEP(4) FA_QK_STEP(6) "}" ::"r"(d_tmem), "l"(qdesc),
+                 "l"(kdesc), "r"(idesc), "r"(0u)
+                 : "memory");
+  }
+}
+__device__ __forceinline__ void mma_pv_product(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc, uint32_t idesc,
+                                               uint32_t acc) {
+  asm volatile(FA_MMA_HEAD FA_PV_FIRST FA_PV_STEP(8, 128) FA_PV_STEP(16, 256) FA_PV_STEP(24, 384) FA_PV_STEP(32, 512)
+                   FA_PV_STEP(40, 640) FA_PV_STEP(48, 768) FA_PV_STEP(56, 896) "}" ::"r"(d_tmem),
+               "r"(p_tmem), "l"(vdesc), "r"(idesc), "r"(acc)
+               : "memory");
+}
+#undef FA_MMA_HEAD
+#undef FA_QK_FIRST
+#undef FA_QK_STEP
+#undef FA_PV_FIRST
+#undef FA_PV_STEP
+
 template <int D, int SK>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc5_kernel(const __grid_constant__ Tc5Params P, const __grid_constant__ CUtensorMap tmQ,
@@ -211,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* const bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* const bar_q = bars;          // [2] Q tile landed
   uint64_t* const bar_s = bars + 2;      // [2] S = Q K^T complete
-  uint64_t* const bar_p = bars + 4;      // [2] P stored in tensor memory (every softmax thread arrives)
+  uint64_t* const bar_p = bars + 4;      // [2] P stored in tensor memory (each softmax warp arrives once)
   uint64_t* const bar_o = bars + 6;      // [2] O += P V complete
   uint64_t* const bar_full = bars + 8;   // [NST] ring slot landed
   uint64_t* const bar_empty = bars + 8 + NST;  // [NST] ring slot consumed
@@ -221,6 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t& s_abort = *(reinterpret_cast<int32_t*>(bars + 10 + 2 * NST) + 1);
   // union summary from the MMA warp: elements, each tile's last element (-1: none), tile 1 visits tile 0's last
   volatile int32_t* const s_info = reinterpret_cast<volatile int32_t*>(bars + 11 + 2 * NST);
+  // per ring slot holding a K tile: which tiles visit its element (bits 0, 1) and whether it is the union's last
+  // (bit 2); written by the producer before the slot's load is armed, read by the MMA warp after it landed
+  volatile int32_t* const s_uflag = reinterpret_cast<volatile int32_t*>(bars + 13 + 2 * NST);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (smem_u32(smem) & 1023u) {  // uniform across the CTA, before any barrier or allocation
@@ -246,8 +329,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   int issued = 0;
   Union uw;            // producer: the union walk
   int c_cur = -1;      // producer: column of the last K load
-  auto load_slot = [&](bool is_v, int c) {  // into the next slot, which must be free
+  auto load_slot = [&](bool is_v, int c, int fl) {  // into the next slot, which must be free
     const int s = issued % NST;
+    if (!is_v) {
+      if (lane == 0) s_uflag[s] = fl;
+      __syncwarp();
+    }
     int yk = c * 128, zk = b * a.Hkv + T0.hk;
     if (a.page_table) {  // key block c is one whole page; a bad page id is reported and page 0 read instead
       int pg = __ldg(a.page_table + (size_t)b * a.max_pages + c);
@@ -274,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < 2; ++t) {
         mbar_init(&bar_q[t], 1);
         mbar_init(&bar_s[t], 1);
-        mbar_init(&bar_p[t], 128);  // every thread of the tile's softmax warpgroup
+        mbar_init(&bar_p[t], 4);  // one lane of each warp of the tile's softmax warpgroup
         mbar_init(&bar_o[t], 1);
       }
       for (int s = 0; s < NST; ++s) {
@@ -308,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!uw.done()) {  // K of the first element (the ring has more slots than this)
       bool i0, i1;
       c_cur = uw.take(T0, T1, desc, i0, i1);
-      load_slot(false, c_cur);
+      load_slot(false, c_cur, (int)i0 | ((int)i1 << 1) | (uw.done() ? 4 : 0));
     }
   }
   if (warp == kMmaWarp) {
@@ -342,20 +429,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     bool ok = true;
-    auto load = [&](bool is_v, int c) -> bool {
+    auto load = [&](bool is_v, int c, int fl) -> bool {
       const int s = issued % NST;
       if (issued >= NST &&
           !__all_sync(0xFFFFFFFFu, mbar_wait(&bar_empty[s], (uint32_t)(((issued / NST) - 1) & 1), wc)))
         return false;
-      load_slot(is_v, c);
+      load_slot(is_v, c, fl);
       return true;
     };
     while (c_cur >= 0 && ok) {
-      ok = load(true, c_cur);
+      ok = load(true, c_cur, 0);
       if (!ok || uw.done()) break;
       bool i0, i1;
       c_cur = uw.take(T0, T1, desc, i0, i1);
-      ok = load(false, c_cur);
+      ok = load(false, c_cur, (int)i0 | ((int)i1 << 1) | (uw.done() ? 4 : 0));
     }
     if (a.counters && lane == 0) {
       unsigned long long* cnt = reinterpret_cast<unsigned long long*>(a.counters);
@@ -373,15 +460,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // =============================== MMA issuer ===============================
-    // Warp-uniform like the producer; each tcgen05.mma / commit is issued by one elected lane.
-    // Descriptors: base values computed once, per-MMA offsets added to the 14-bit address field.
+    // Warp-uniform like the producer; each product (all its K-steps) and each commit is issued by one
+    // elected lane. Descriptors: base values computed once, per-K-step offsets added to the address field.
     // Order: at union step k, for tile 0 then tile 1 (each only on its own elements), O_t += P_t(u_k-1)
     // V(u_k-1) once P_t is ready, then S_t = Q_t K(u_k)^T. The tensor pipe runs one thread's MMAs in issue
     // order, so S_t overwrites P_t only after the product has read it, and the completion of S_t implies
     // that of O_t's previous update. Waiting for P_0 before P_1 keeps the two tiles' softmaxes apart: each
     // runs while the tensor core works on the other tile. A ring slot is released (commit to its "empty"
-    // barrier) after the last product that reads it.
-    constexpr int CW = 128;  // keys whose P one softmax thread writes (the whole block)
+    // barrier) after the last product that reads it. Which tiles visit an element, and whether it is the last,
+    // come with its K slot (flags written by the producer): this warp does not walk the block lists, and
+    // between two products it only waits on barriers (walking them here cost the tensor core 2-4 %).
     constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
     const uint64_t qdesc0 = sdesc_sw128(smem_u32(sQ0), 16, 1024), qdesc1 = sdesc_sw128(smem_u32(sQ1), 16, 1024);
@@ -402,20 +490,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto mma_qk = [&](int t, int s) {
       const uint64_t qd = t ? qdesc1 : qdesc0;
       const uint64_t kd = kdesc + (uint64_t)(s * (C::kSlotBytes >> 4));
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-        tc5_mma_ss_elect(tmem + C::col_s(t), qd + off, kd + off, idesc_qk, ks > 0 ? 1u : 0u);
-      }
+      mma_qk_product<D / 16>(tmem + C::col_s(t), qd, kd, idesc_qk);
       tc5_commit_elect(&bar_s[t]);
     };
     auto mma_pv = [&](int t, int s, bool acc) {
       const uint64_t vd = vdesc + (uint64_t)(s * (C::kSlotBytes >> 4));
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)  // keys 16 ks .. + 15: P of column group 16 ks / CW, over its first columns
-        tc5_mma_ts_elect(tmem + C::col_o(t), tmem + C::col_s(t) + (uint32_t)(CW * (16 * ks / CW) + (16 * ks % CW) / 2),
-                         vd + (uint64_t)((ks * 2048) >> 4),
-                         idesc_pv, (acc || ks > 0) ? 1u : 0u);
+      mma_pv_product(tmem + C::col_o(t), tmem + C::col_s(t), vd, idesc_pv, acc ? 1u : 0u);
       tc5_commit_elect(&bar_o[t]);
     };
     auto wait_p = [&](int t, int j) -> bool {
@@ -428,22 +508,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int sk, sv;  // ring slots of the element's K and V
     };
     Step cur{false, false, false, -1, -1}, prev = cur;
-    Union mw;
-    mw.init(T0, T1, desc);
+    bool more = T0.n + T1.n > 0;  // an element of the union is still to come
     int np[2] = {0, 0};  // P blocks consumed so far per tile
     int uk = 0, last0 = -1, last1 = -1, both0 = 0;  // union elements taken; each tile's last; tile 1 on last0
     bool info = false;
     while (ok) {
-      cur.live = !mw.done();
-      if (cur.live) {
-        mw.take(T0, T1, desc, cur.in0, cur.in1);
-        if (cur.in0) {
-          last0 = uk;
-          both0 = cur.in1;
-        }
-        if (cur.in1) last1 = uk;
-        ++uk;
-      } else if (!info) {  // the union is known: its summary for the epilogues' staging plans
+      cur.live = more;
+      if (!cur.live && !info) {  // the union is known: its summary for the epilogues' staging plans
         if (lane == 0) {
           s_info[0] = uk;
           s_info[1] = last0;
@@ -458,7 +529,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // slots of V(prev) and K(cur), taken before the waits for P, so that their barrier waits are off the
       // path from P to the next products
       if (prev.live && (prev.sv = take()) < 0) { ok = false; break; }
-      if (cur.live && (cur.sk = take()) < 0) { ok = false; break; }
+      if (cur.live) {
+        if ((cur.sk = take()) < 0) { ok = false; break; }
+        const int fl = s_uflag[cur.sk];
+        cur.in0 = fl & 1;
+        cur.in1 = (fl >> 1) & 1;
+        more = !(fl & 4);
+        if (cur.in0) {
+          last0 = uk;
+          both0 = cur.in1;
+        }
+        if (cur.in1) last1 = uk;
+        ++uk;
+      }
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const bool use_v = prev.live && (t ? prev.in1 : prev.in0);
@@ -663,7 +746,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc5_wait_st();
         tc5_fence_before();
-        mbar_arrive(&bar_p[t]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_p[t]);
       }
       // ---- epilogue: wait for the tile's last O update, normalise and store
       ok = __all_sync(0xFFFFFFFFu, ok);
