@@ -42,6 +42,12 @@ constexpr int kThreads = 10 * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 2^8
+// A soft-capped score lies in (-c, c), so its exponent x log2(e) c spans less than 2 c log2(e): with the
+// fixed reference c log2(e) - 64, P = 2^(x log2(e) c - m) stays within [2^(64 - 2 c log2(e)), 2^64], normal in
+// fp32 and bf16 (and O, a sum of at most 2^31 such P times bf16 V, far from overflow) for c log2(e) <= 90.
+// The softmax then needs no running maximum: no max pass before P, no O rescale.
+constexpr float kCapFixedMax = 90.0f;   // largest c log2(e) that takes the fixed reference
+constexpr float kCapFixedSpan = 64.0f;  // P <= 2^64
 
 enum ScoreKind { SK_NONE = 0, SK_ALIBI = 1, SK_SOFTCAP = 2, SK_GENERIC = 3 };
 
@@ -600,7 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (SK == SK_ALIBI || SK == SK_GENERIC) slope2 = a.score.alibi ? __ldg(a.score.alibi + TT.h) * kLog2e : 0.f;
       // the factor the exponent's FMA applies: the scale (no score rule) or log2(e) c (soft-cap), else 1
       const float mult = SK == SK_NONE ? sl2 : SK == SK_SOFTCAP ? a.score.softcap * kLog2e : 1.f;
-      float m_ref = -INFINITY;  // reference max (log2 domain) used for P and for O
+      // reference max (log2 domain) used for P and for O; fixed for soft-capped scores
+      float m_ref = SK == SK_SOFTCAP ? mult - kCapFixedSpan : -INFINITY;
       // the row sum of P (for the LSE), and the correction that turns it into the sum O is divided by: per
       // block, the bf16 rounding error of the row's largest P (see the P loop)
       float le = 0.f, lc = 0.f;
@@ -683,20 +690,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) x[k * 32 + i] = ((wd >> i) & 1u) ? x[k * 32 + i] : -INFINITY;
           }
         }
-        // ---- the row's block max: 4 independent chains of 3-input maxima
-        float mxk[4];
+        // ---- the row's block max: 4 independent chains of 3-input maxima (with the fixed reference of a
+        // soft-cap, taken inside the P loop instead: only the correction term below needs it)
+        float mxk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (SK != SK_SOFTCAP) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mxk[k] = fmaxf(x[k], x[k + 4]);
+          for (int k = 0; k < 4; ++k) mxk[k] = fmaxf(x[k], x[k + 4]);
 #pragma unroll
-        for (int i = 8; i < 128; i += 8)
+          for (int i = 8; i < 128; i += 8)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) mxk[k] = fmax3(mxk[k], x[i + k], x[i + 4 + k]);
-        const float xmax = fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3]));
+            for (int k = 0; k < 4; ++k) mxk[k] = fmax3(mxk[k], x[i + k], x[i + 4 + k]);
+        }
+        float xmax = fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3]));
         const float mb = xmax * mult;
         // ---- reference max: move it only when the block max exceeds it by more than 2^8
         float alpha = 1.f;
         bool rescale = false;
-        if (mb > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mb > -INFINITY)) {
+        if (SK != SK_SOFTCAP && (mb > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mb > -INFINITY))) {
           alpha = m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - mb);
           rescale = j > 0 && m_ref != -INFINITY;
           m_ref = mb;
@@ -720,11 +730,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             float y0, y1;
             f2_unpack(f2_fma(f2_pack(x[16 * ch + 2 * i], x[16 * ch + 2 * i + 1]), mul2, neg2), y0, y1);
             const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+            if (SK == SK_SOFTCAP) mxk[i & 3] = fmax3(mxk[i & 3], x[16 * ch + 2 * i], x[16 * ch + 2 * i + 1]);
             pk[i] = pack_bf16x2(p0, p1);
             se[i & 1] = f2_add(se[i & 1], f2_pack(p0, p1));
           }
           tc5_st8(tS + 8 * ch, pk);
         }
+        if (SK == SK_SOFTCAP) xmax = fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3]));
         const float ph = ex2_approx(fmaf(xmax, mult, -mr));
         const float ch_err = __uint_as_float(pack_bf16x2(ph, 0.f) << 16) - ph;
         float e0, e1;
@@ -753,7 +765,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar_o[t], (uint32_t)((TT.n - 1) & 1), wc));
       tc5_fence_after();
-      const bool empty = m_ref == -INFINITY;
+      // no key of the row visible: no reference max, or (fixed reference) a zero sum, every P of a visible
+      // key being at least 2^(64 - 2 c log2(e)) > 0
+      const bool empty = SK == SK_SOFTCAP ? le == 0.f : m_ref == -INFINITY;
       const float inv = empty ? 0.f : 1.f / (le + lc);
       if (ok && q_row < a.q_len) Lg[o_row] = empty ? -INFINITY : (m_ref + __log2f(le)) * kLn2;
       // fp32 O ([128][D], D / 32 boxes of [128][32]: 128-byte rows, 128-byte swizzle; two ring slots) is
@@ -927,7 +941,7 @@ int launch_sk(const FwdArgs& a, cudaStream_t st) {
   const bool al = a.score.alibi != nullptr, rel = a.score.rel != nullptr, cap = a.score.softcap > 0.f;
   if (!al && !rel && !cap) return launch_k<D, SK_NONE>(a, st);
   if (al && !rel && !cap) return launch_k<D, SK_ALIBI>(a, st);
-  if (!al && !rel && cap) return launch_k<D, SK_SOFTCAP>(a, st);
+  if (!al && !rel && cap && a.score.softcap * kLog2e <= kCapFixedMax) return launch_k<D, SK_SOFTCAP>(a, st);
   return launch_k<D, SK_GENERIC>(a, st);
 }
 

@@ -60,6 +60,11 @@ CASES = [
     ("causal_9_pairs", 3, 6, 6, 384, 384, 128, 128, 128, [("causal",)], {}),
     ("gqa_12_pairs_softcap", 2, 12, 4, 384, 384, 128, 128, 128, CW(200), dict(softcap=30.0)),
     ("window_mha_10_heads", 2, 5, 5, 512, 512, 128, 128, 128, CW(256), {}),
+    # soft-cap with the fixed reference maximum: rows that see no key at all (queries past the keys' window)
+    # must still come out empty; a cap too large for the fixed reference (c log2(e) > 90) takes the
+    # generic score path
+    ("softcap_empty_rows", 1, 2, 2, 300, 100, 128, 128, 128, [("window", 50)], dict(softcap=30.0)),
+    ("softcap_large_cap", 1, 2, 2, 400, 400, 128, 128, 128, CW(200), dict(softcap=80.0)),
 ]
 
 
