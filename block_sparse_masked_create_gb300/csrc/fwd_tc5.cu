@@ -13,15 +13,18 @@
 //                    % 4) + lane) over all 128 key columns of a block, so no value is exchanged between
 //                    threads. Per block: S from TMEM to registers, score rule, mask (partial blocks only),
 //                    row max, P = 2^(x - m) with packed fp32x2 FMAs, the row sum, P as bf16 back into
-//                    tensor memory over the S columns it came from, "P ready". The O accumulator is
-//                    rescaled in TMEM only when the running max grows by more than 2^8 (exact for any
-//                    reference max; the bound keeps P <= 256). Epilogue O / l -> shared memory -> TMA store.
+//                    tensor memory over the S columns it came from, "P ready" (one arrival per warp). The
+//                    O accumulator is rescaled in TMEM only when the running max grows by more than 2^8
+//                    (exact for any reference max; the bound keeps P <= 256); soft-capped scores take a
+//                    fixed reference and no max pass. Epilogue O / l -> shared memory -> TMA store.
 //   warp 8           TMA producer: Q tiles, then K / V tiles of the union of the two tiles' block lists
 //                    (each block once; an empty block issues no load) into a shared-memory ring, in the
-//                    order the MMA warp consumes them.
+//                    order the MMA warp consumes them; with each K tile, the element's flags (which tiles
+//                    visit it, whether it is the last), so the MMA warp does not walk the lists.
 //   warp 9           allocates TMEM (S/P and O of both tiles: 512 columns) and issues every tcgen05.mma from
 //                    one thread: per element of the union, for each tile that visits it, O_t += P_t V(prev)
-//                    (A read from TMEM) once P_t is ready and then S_t = Q_t K^T (A, B from shared memory).
+//                    (A read from TMEM) once P_t is ready and then S_t = Q_t K^T (A, B from shared memory),
+//                    each product one asm statement under one elect.
 //                    The tensor pipe runs a thread's MMAs in issue order, so S_t overwrites P_t only after
 //                    the product has read it, and the completion of S_t implies that of O_t's previous update.
 // Each tile's softmax runs while the tensor core works on the other tile. Every wait is bounded (an abort
