@@ -102,7 +102,10 @@ typedef struct {
 typedef struct {
   const float* alibi_slopes; /* device fp32 [Hq] or NULL:  s += -slope[h] * (i - j) */
   const float* rel_bias;     /* device fp32 [Hq, 2*KV_LEN-1] or NULL:  s += rel_bias[h][(i - j) + KV_LEN - 1] */
-  float softcap;             /* > 0: s = softcap * tanh(s / softcap);  <= 0: off */
+  float softcap;             /* > 0: s = softcap * tanh(s / softcap);  <= 0: off. The 128x128 forward
+                                specialises the soft-cap alone for softcap <= 62.3 (a fixed softmax
+                                reference; see fa_flex_forward); a larger cap, or a cap with a bias,
+                                takes its generic score path (same results, slower). */
 } fa_score_rule;
 
 /* ------------------------------------------------------------------------------------------------
@@ -201,7 +204,11 @@ typedef enum { FA_OUT_BF16 = 0, FA_OUT_F32 = 1 } fa_out_dtype;
  *                tile of the CTA that reads it (sibling query heads of one KV head with one mask row).
  * Supported: d in {64, 128}; Bq, Bk in {16, 32, 64, 128}; Q_LEN, KV_LEN >= 1; Hq % Hkv == 0;
  * q/k/v/out 16-byte aligned. Bq == Bk == 128 runs the tcgen05/TMEM kernel, other block sizes the
- * mma.sync kernel. */
+ * mma.sync kernel. The softmax reference m of a row is the running maximum, moved only when a block
+ * exceeds it by 2^8 in log2 units, except under a soft-cap alone with softcap <= 62.3 on the tcgen05
+ * kernel: the scores then lie in (-c, c) and m is fixed at c log2(e) - 64 (log2 units), every P staying
+ * a normal fp32/bf16 number in [2^(64 - 2c log2 e), 2^64]. Either way LSE = m + ln l is exact up to
+ * rounding. */
 FA_API fa_status fa_flex_forward(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
                                  const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype,
                                  float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t Q_LEN, int32_t KV_LEN,
