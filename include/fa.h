@@ -207,7 +207,7 @@ typedef enum { FA_OUT_BF16 = 0, FA_OUT_F32 = 1 } fa_out_dtype;
  * mma.sync kernel. The softmax reference m of a row is the running maximum, moved only when a block
  * exceeds it by 2^8 in log2 units, except under a soft-cap alone with softcap <= 62.3 on the tcgen05
  * kernel: the scores then lie in (-c, c) and m is fixed at c log2(e) - 64 (log2 units), every P staying
- * a normal fp32/bf16 number in [2^(64 - 2c log2 e), 2^64]. Either way LSE = m + ln l is exact up to
+ * a normal fp32/bf16 number in [2^(64 - 2c log2 e), 2^64]. The choice of m changes O and LSE only by
  * rounding. */
 FA_API fa_status fa_flex_forward(const void* q, const void* k, const void* v, const fa_block_mask* block_mask,
                                  const fa_score_rule* score_rule, float scale, void* out, int32_t out_dtype,
